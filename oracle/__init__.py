@@ -1,0 +1,184 @@
+"""CPU oracle for the block-glue path (LN, residual add + LN, window index
+map, window gather, norm-gather, bias + tanh-GELU).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+benchmark's CPU-baseline leg import this package; the library in
+``window_gather_swin_gb300`` never does, and shares no code with it.
+
+The arithmetic lives in ``wgs_oracle.c`` (plain C, double precision, one
+element at a time).  This module only marshals numpy arrays through ctypes.
+fp16 tensors are passed as ``numpy.float16`` arrays and handled as their
+binary16 bit patterns.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        sig = {
+            "orc_f16_to_f64": (ctypes.c_double, [ctypes.c_uint16]),
+            "orc_rn16": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_rn16_array": (None, [P, P, i64]),
+            "orc_f16_to_f64_array": (None, [P, P, i64]),
+            "orc_ln_row_f64": (None, [P, P, i32, f32]),
+            "orc_ln": (None, [P, P, i64, i32, f32]),
+            "orc_ln_f64": (None, [P, P, i64, i32, f32]),
+            "orc_residual_add_ln": (None, [P, P, P, P, i64, i32, f32]),
+            "orc_window_index_count": (i64, [P, P, P]),
+            "orc_build_window_index": (ctypes.c_int, [P, P, P, P, i32, P]),
+            "orc_window_gather": (i64, [P, P, P, i64, i64, i32]),
+            "orc_norm_gather": (i64, [P, P, P, i64, i64, i32, f32]),
+            "orc_bias_gelu_f32": (None, [P, P, P, P, i64, i32]),
+            "orc_bias_gelu_f16": (None, [P, P, P, P, i64, i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _i3(v):
+    return None if v is None else np.ascontiguousarray(np.asarray(v, dtype=np.int32).reshape(3))
+
+
+# ---------------------------------------------------------------- fp16 ----
+
+def rn16(values) -> np.ndarray:
+    """Round doubles to binary16 (nearest, ties to even); returns float16."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().orc_rn16_array(_ptr(v), _ptr(out), v.size)
+    return out.view(np.float16)
+
+
+def f16_to_f64(values) -> np.ndarray:
+    """Exact double value of each binary16 element."""
+    b = np.ascontiguousarray(values, dtype=np.float16).view(np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().orc_f16_to_f64_array(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+# ------------------------------------------------------------------ LN ----
+
+def ln_row_f64(x, eps: float = 1e-5) -> np.ndarray:
+    """Unrounded LN of one row of doubles."""
+    x = _c(x, np.float64).ravel()
+    y = np.empty_like(x)
+    _load().orc_ln_row_f64(_ptr(x), _ptr(y), x.size, eps)
+    return y
+
+
+def ln(x, eps: float = 1e-5) -> np.ndarray:
+    """No-affine LayerNorm of fp16 rows [rows, width] -> fp16."""
+    x = _c(x, np.float16)
+    rows, width = x.shape
+    y = np.empty_like(x)
+    _load().orc_ln(_ptr(x), _ptr(y), rows, width, eps)
+    return y
+
+
+def ln_f64(x, eps: float = 1e-5) -> np.ndarray:
+    """Unrounded (double) LN outputs of fp16 rows."""
+    x = _c(x, np.float16)
+    rows, width = x.shape
+    y = np.empty(x.shape, dtype=np.float64)
+    _load().orc_ln_f64(_ptr(x), _ptr(y), rows, width, eps)
+    return y
+
+
+def residual_add_ln(residual, branch, eps: float = 1e-5):
+    """Returns (residual_out, y), both fp16."""
+    a = _c(residual, np.float16)
+    b = _c(branch, np.float16)
+    assert a.shape == b.shape and a.ndim == 2
+    r = np.empty_like(a)
+    y = np.empty_like(a)
+    _load().orc_residual_add_ln(_ptr(a), _ptr(b), _ptr(r), _ptr(y), a.shape[0], a.shape[1], eps)
+    return r, y
+
+
+# ----------------------------------------------------------- index map ----
+
+def window_index_count(grid, win, padded=None) -> int:
+    n = _load().orc_window_index_count(_ptr(_i3(grid)), _ptr(_i3(win)), _ptr(_i3(padded)))
+    if n < 0:
+        raise ValueError("invalid grid/window/padded extents")
+    return int(n)
+
+
+def build_window_index(grid, win, shift, padded=None, flags: int = 0) -> np.ndarray:
+    """INT32 destination->source map; -1 marks a pad row."""
+    n = window_index_count(grid, win, padded)
+    out = np.empty(n, dtype=np.int32)
+    rc = _load().orc_build_window_index(_ptr(_i3(grid)), _ptr(_i3(win)), _ptr(_i3(shift)),
+                                        _ptr(_i3(padded)), flags, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_build_window_index failed ({rc})")
+    return out
+
+
+# -------------------------------------------------------------- gather ----
+
+def window_gather(src, idx):
+    """Returns (dst, number of indices outside [-1, n_src))."""
+    s = _c(src, np.float16)
+    i = _c(idx, np.int32).ravel()
+    dst = np.empty((i.size, s.shape[1]), dtype=np.float16)
+    bad = _load().orc_window_gather(_ptr(s), _ptr(i), _ptr(dst), s.shape[0], i.size, s.shape[1])
+    return dst, int(bad)
+
+
+def norm_gather(src, idx, eps: float = 1e-5):
+    """Returns (dst, number of indices outside [-1, n_src))."""
+    s = _c(src, np.float16)
+    i = _c(idx, np.int32).ravel()
+    dst = np.empty((i.size, s.shape[1]), dtype=np.float16)
+    bad = _load().orc_norm_gather(_ptr(s), _ptr(i), _ptr(dst), s.shape[0], i.size, s.shape[1], eps)
+    return dst, int(bad)
+
+
+# ---------------------------------------------------------------- GELU ----
+
+def bias_gelu_tanh(x, bias, want_f64: bool = True):
+    """Returns (y, y64): y in the dtype of x (float32 or float16), y64 the
+    unrounded double result (None unless want_f64)."""
+    x = np.asarray(x)
+    lib = _load()
+    if x.dtype == np.float32:
+        xs, bs = _c(x, np.float32), _c(bias, np.float32)
+        fn = lib.orc_bias_gelu_f32
+    elif x.dtype == np.float16:
+        xs, bs = _c(x, np.float16), _c(bias, np.float16)
+        fn = lib.orc_bias_gelu_f16
+    else:
+        raise TypeError("bias_gelu_tanh oracle takes float32 or float16")
+    rows, width = xs.shape
+    assert bs.shape == (width,)
+    y = np.empty_like(xs)
+    y64 = np.empty(xs.shape, dtype=np.float64) if want_f64 else None
+    fn(_ptr(xs), _ptr(bs), _ptr(y), _ptr(y64), rows, width)
+    return y, y64

@@ -1,0 +1,343 @@
+/*
+ * CPU oracle for the shifted-window transformer block-glue path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library: every step below is written out from the definition it
+ * cites, in double precision, one element at a time, with no blocking,
+ * fusion or reordering.
+ *
+ * Sources (page title, section):
+ *   [P1] "BW1000 gfx936 Pangu-Weather inference profiling" (l189.com news
+ *        2144533): s3 fixed-width LayerNorm, s4 residual add + norm and its
+ *        FP16 rounding point, s5 window gather with the INT32 index protocol
+ *        and the fused norm-gather.
+ *   [P3] "PyTorch + HIP fused bias + GELU on Hygon DCU" (forum.sourcefind.cn):
+ *        s3 math semantics (tanh-approximate GELU of input + bias).
+ *
+ * fp16 values travel as their IEEE binary16 bit patterns (uint16_t).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* ------------------------------------------------------------------ */
+/* IEEE-754 binary16 <-> double                                        */
+/* ------------------------------------------------------------------ */
+
+/* Exact value of a binary16 bit pattern (IEEE 754-2008, s3.4). */
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);             /* subnormal or zero */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* Round q >= 0 (an integer plus a fraction, exactly representable) to the
+ * nearest integer, ties to the even integer. */
+static double round_half_even(double q)
+{
+    double fl = floor(q);
+    double frac = q - fl;
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* double -> binary16 bits, round to nearest, ties to even (IEEE 754-2008
+ * s4.3.1).  Overflow goes to infinity, tiny values to subnormals or zero,
+ * NaN stays NaN (quiet), the sign of zero is kept. */
+uint16_t orc_rn16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return (uint16_t)(sign | 0x7E00);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00);
+    /* 65504 is the largest finite value; the midpoint between it and 2^16
+     * is 65520, and a tie there goes to the even neighbour 2^16 = inf. */
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: the quantum is 2^-24 */
+        double n = round_half_even(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)n); /* n == 1024 encodes 2^-14 */
+    }
+    int ex;
+    double m = frexp(a, &ex);       /* a = m * 2^ex, m in [0.5, 1) */
+    int E = ex - 1;                 /* a = (2m) * 2^E, 2m in [1, 2) */
+    double n = round_half_even(ldexp(a, 10 - E)); /* in [1024, 2048] */
+    if (n == 2048.0) { n = 1024.0; E += 1; }
+    if (E + 15 >= 31) return (uint16_t)(sign | 0x7C00);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(n - 1024.0));
+}
+
+/* Element-wise forms of the two conversions above. */
+void orc_rn16_array(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_rn16(v[i]);
+}
+
+void orc_f16_to_f64_array(const uint16_t *h, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_f64(h[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* LayerNorm without affine  [P1 s3]                                   */
+/* ------------------------------------------------------------------ */
+
+/* One row, unrounded: y = (x - mean) / sqrt(var + eps) with the biased
+ * (divide by width) variance, both statistics taken in two passes.  eps
+ * is the single-precision value the caller passes. */
+void orc_ln_row_f64(const double *x, double *y, int32_t width, float eps)
+{
+    double mean = 0.0;
+    for (int32_t i = 0; i < width; ++i) mean += x[i];
+    mean /= (double)width;
+    double var = 0.0;
+    for (int32_t i = 0; i < width; ++i) {
+        double d = x[i] - mean;
+        var += d * d;
+    }
+    var /= (double)width;
+    double denom = sqrt(var + (double)eps);
+    for (int32_t i = 0; i < width; ++i) y[i] = (x[i] - mean) / denom;
+}
+
+/* fp16 rows in, fp16 rows out: each output is the rounding of the exact
+ * (double) normalised value. */
+void orc_ln(const uint16_t *x, uint16_t *y, int64_t rows, int32_t width, float eps)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)width);
+    double *yd = (double *)malloc(sizeof(double) * (size_t)width);
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * (int64_t)width;
+        for (int32_t i = 0; i < width; ++i) xd[i] = orc_f16_to_f64(xr[i]);
+        orc_ln_row_f64(xd, yd, width, eps);
+        for (int32_t i = 0; i < width; ++i) y[r * (int64_t)width + i] = orc_rn16(yd[i]);
+    }
+    free(xd);
+    free(yd);
+}
+
+/* Unrounded LN outputs of fp16 rows, for tolerance decisions. */
+void orc_ln_f64(const uint16_t *x, double *y, int64_t rows, int32_t width, float eps)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)width);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int32_t i = 0; i < width; ++i) xd[i] = orc_f16_to_f64(x[r * (int64_t)width + i]);
+        orc_ln_row_f64(xd, y + r * (int64_t)width, width, eps);
+    }
+    free(xd);
+}
+
+/* ------------------------------------------------------------------ */
+/* Residual add + LayerNorm  [P1 s4]                                   */
+/* ------------------------------------------------------------------ */
+
+/* residual_out = fp16(residual + branch); y = LN(residual_out), taken from
+ * the rounded fp16 value.  The page states the sum as fp16(fp32 a + fp32 b);
+ * the sum of two binary16 values is exact in double, and since binary32
+ * carries 24 >= 2*11 + 2 significand bits, rounding first to binary32 and
+ * then to binary16 gives the same result as rounding the exact sum once
+ * (Figueroa, "When is double rounding innocuous?", 1995). */
+void orc_residual_add_ln(const uint16_t *a, const uint16_t *b, uint16_t *r_out, uint16_t *y,
+                         int64_t rows, int32_t width, float eps)
+{
+    int64_t n = rows * (int64_t)width;
+    for (int64_t i = 0; i < n; ++i)
+        r_out[i] = orc_rn16(orc_f16_to_f64(a[i]) + orc_f16_to_f64(b[i]));
+    orc_ln(r_out, y, rows, width, eps);
+}
+
+/* ------------------------------------------------------------------ */
+/* Shifted-window index map  [P1 s5]                                   */
+/* ------------------------------------------------------------------ */
+/*
+ * The page fixes the protocol (one INT32 per destination row; a value >= 0
+ * names the source token, -1 asks for a zero row) but not the construction.
+ * The reading taken here:
+ *   - tokens are the row-major flattening of a (Z, H, W) grid;
+ *   - the padded grid has extents padded[] (each >= the grid extent), by
+ *     default each extent rounded up to a multiple of the window;
+ *   - windows tile the padded grid from the origin; where a padded extent is
+ *     not a multiple of the window, the last window on that axis is cut short;
+ *   - destination rows are ordered window by window (row-major over the
+ *     window grid), then row-major over the cells inside each window;
+ *   - flags == 0 (shift, then pad): a cell (z,h,w) inside the original grid
+ *     reads source ((z+sz) mod Z, (h+sh) mod H, (w+sw) mod W), a cyclic roll
+ *     by -shift; cells outside it are pads (-1);
+ *   - flags == 1 (pad, then shift): the roll runs over the padded grid and a
+ *     cell whose rolled position falls outside the original grid is a pad.
+ *
+ * This builder scatters: for every padded cell it computes where that cell
+ * lands in the destination order.
+ */
+
+static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t pos_mod(int64_t a, int64_t m) { int64_t r = a % m; return r < 0 ? r + m : r; }
+
+static int resolve_padded(const int32_t grid[3], const int32_t win[3], const int32_t *padded,
+                          int64_t P[3])
+{
+    for (int k = 0; k < 3; ++k) {
+        if (grid[k] < 1 || win[k] < 1) return -1;
+        P[k] = padded ? (int64_t)padded[k] : ceil_div64(grid[k], win[k]) * win[k];
+        if (P[k] < grid[k]) return -1;
+    }
+    return 0;
+}
+
+int64_t orc_window_index_count(const int32_t grid[3], const int32_t win[3], const int32_t *padded)
+{
+    int64_t P[3];
+    if (resolve_padded(grid, win, padded, P) != 0) return -1;
+    return P[0] * P[1] * P[2];
+}
+
+int orc_build_window_index(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                           const int32_t *padded, int32_t flags, int32_t *out)
+{
+    int64_t P[3];
+    if (resolve_padded(grid, win, padded, P) != 0) return -1;
+    if (flags != 0 && flags != 1) return -1;
+    const int64_t Z = grid[0], H = grid[1], W = grid[2];
+    int64_t nwin[3];
+    for (int k = 0; k < 3; ++k) nwin[k] = ceil_div64(P[k], win[k]);
+
+    /* size of every window, then where each window starts in the output */
+    int64_t n_windows = nwin[0] * nwin[1] * nwin[2];
+    int64_t *start = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_windows + 1));
+    if (!start) return -2;
+    start[0] = 0;
+    for (int64_t bz = 0; bz < nwin[0]; ++bz)
+        for (int64_t bh = 0; bh < nwin[1]; ++bh)
+            for (int64_t bw = 0; bw < nwin[2]; ++bw) {
+                int64_t ez = P[0] - bz * win[0]; if (ez > win[0]) ez = win[0];
+                int64_t eh = P[1] - bh * win[1]; if (eh > win[1]) eh = win[1];
+                int64_t ew = P[2] - bw * win[2]; if (ew > win[2]) ew = win[2];
+                int64_t w_id = (bz * nwin[1] + bh) * nwin[2] + bw;
+                start[w_id + 1] = start[w_id] + ez * eh * ew;
+            }
+
+    for (int64_t z = 0; z < P[0]; ++z)
+        for (int64_t h = 0; h < P[1]; ++h)
+            for (int64_t w = 0; w < P[2]; ++w) {
+                int64_t bz = z / win[0], bh = h / win[1], bw = w / win[2];
+                int64_t iz = z % win[0], ih = h % win[1], iw = w % win[2];
+                int64_t eh = P[1] - bh * win[1]; if (eh > win[1]) eh = win[1];
+                int64_t ew = P[2] - bw * win[2]; if (ew > win[2]) ew = win[2];
+                int64_t w_id = (bz * nwin[1] + bh) * nwin[2] + bw;
+                int64_t dst = start[w_id] + (iz * eh + ih) * ew + iw;
+
+                int64_t src = -1;
+                if (flags == 0) {
+                    if (z < Z && h < H && w < W) {
+                        int64_t zs = pos_mod(z + shift[0], Z);
+                        int64_t hs = pos_mod(h + shift[1], H);
+                        int64_t ws = pos_mod(w + shift[2], W);
+                        src = (zs * H + hs) * W + ws;
+                    }
+                } else {
+                    int64_t zs = pos_mod(z + shift[0], P[0]);
+                    int64_t hs = pos_mod(h + shift[1], P[1]);
+                    int64_t ws = pos_mod(w + shift[2], P[2]);
+                    if (zs < Z && hs < H && ws < W) src = (zs * H + hs) * W + ws;
+                }
+                out[dst] = (int32_t)src;
+            }
+    free(start);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Window gather and fused norm-gather  [P1 s5]                        */
+/* ------------------------------------------------------------------ */
+
+/* dst[d] = src[idx[d]] for idx[d] >= 0 (bit copy), an all-zero row for
+ * idx[d] == -1.  Any other index is outside the protocol: the oracle writes
+ * a zero row for it and counts it in the return value. */
+int64_t orc_window_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst,
+                          int64_t n_src, int64_t n_idx, int32_t width)
+{
+    int64_t bad = 0;
+    for (int64_t d = 0; d < n_idx; ++d) {
+        int64_t s = idx[d];
+        int ok = (s >= 0 && s < n_src);
+        if (!ok && s != -1) ++bad;
+        for (int32_t i = 0; i < width; ++i)
+            dst[d * (int64_t)width + i] = ok ? src[s * (int64_t)width + i] : (uint16_t)0;
+    }
+    return bad;
+}
+
+/* dst[d] = LN(src[idx[d]]) for idx[d] >= 0, zero row for -1: the
+ * normalised tensor is defined row by row, so this is LN applied to each
+ * gathered row. */
+int64_t orc_norm_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst,
+                        int64_t n_src, int64_t n_idx, int32_t width, float eps)
+{
+    int64_t bad = 0;
+    for (int64_t d = 0; d < n_idx; ++d) {
+        int64_t s = idx[d];
+        uint16_t *out = dst + d * (int64_t)width;
+        if (s >= 0 && s < n_src) {
+            orc_ln(src + s * (int64_t)width, out, 1, width, eps);
+        } else {
+            if (s != -1) ++bad;
+            for (int32_t i = 0; i < width; ++i) out[i] = 0;
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* Bias + tanh-approximate GELU  [P3 s3]                               */
+/* ------------------------------------------------------------------ */
+
+/* gelu(t) = 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3))) */
+static double gelu_tanh(double t)
+{
+    const double k = sqrt(2.0 / acos(-1.0));
+    return 0.5 * t * (1.0 + tanh(k * (t + 0.044715 * t * t * t)));
+}
+
+/* fp32: t = fp32(x + bias[col]) (the sum of two floats rounded once to
+ * binary32; going through double first is innocuous since 53 >= 2*24 + 2),
+ * y64 = gelu(t) exactly in double, y = fp32(y64). */
+void orc_bias_gelu_f32(const float *x, const float *bias, float *y, double *y64,
+                       int64_t rows, int32_t width)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t c = 0; c < width; ++c) {
+            int64_t i = r * (int64_t)width + c;
+            float t = (float)((double)x[i] + (double)bias[c]);
+            double g = gelu_tanh((double)t);
+            if (y64) y64[i] = g;
+            if (y) y[i] = (float)g;
+        }
+}
+
+/* fp16: t = fp16(x + bias[col]), keeping the rounding point an eager
+ * `gelu(x + bias)` in half precision would have; y = fp16(gelu(t)). */
+void orc_bias_gelu_f16(const uint16_t *x, const uint16_t *bias, uint16_t *y, double *y64,
+                       int64_t rows, int32_t width)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t c = 0; c < width; ++c) {
+            int64_t i = r * (int64_t)width + c;
+            uint16_t t = orc_rn16(orc_f16_to_f64(x[i]) + orc_f16_to_f64(bias[c]));
+            double g = gelu_tanh(orc_f16_to_f64(t));
+            if (y64) y64[i] = g;
+            if (y) y[i] = orc_rn16(g);
+        }
+}

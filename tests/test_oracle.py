@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle against facts fixed outside itself: IEEE binary16
+rounding as numpy implements it, closed forms and invariants of LayerNorm,
+torch's float64 layer_norm and tanh-GELU, hand-derived index-map entries and
+a sort-based brute-force index-map builder.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped eps, an
+unbiased variance, a wrong shift sign, a transposed window order, a bias
+indexed by row, an LN taken before the fp16 rounding point) fails here.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from golden_io import gelu_tiny_input, window_index_cases
+from window_gather_swin_gb300 import synth
+
+EPS = float(np.float32(1e-5))
+
+
+# ------------------------------------------------------------- binary16 ----
+
+def _all_f16():
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+
+
+def test_f16_decode_matches_numpy_on_every_pattern():
+    h = _all_f16()
+    ours = oracle.f16_to_f64(h)
+    ref = h.astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_rn16_round_trips_every_pattern():
+    h = _all_f16()
+    back = oracle.rn16(oracle.f16_to_f64(h))
+    nan = np.isnan(h.astype(np.float64))
+    assert np.array_equal(back.view(np.uint16)[~nan], h.view(np.uint16)[~nan])
+    assert np.isnan(back[nan].astype(np.float64)).all()
+
+
+def test_rn16_matches_numpy_on_random_doubles():
+    rng = np.random.default_rng(11)
+    mag = np.exp2(rng.uniform(-30.0, 17.0, 400_000))
+    v = mag * rng.choice([-1.0, 1.0], mag.size)
+    assert np.array_equal(oracle.rn16(v).view(np.uint16), v.astype(np.float16).view(np.uint16))
+
+
+def test_rn16_ties_go_to_even_and_near_ties_to_nearest():
+    h = _all_f16()
+    vals = h.astype(np.float64)
+    pos = vals[(vals >= 0) & np.isfinite(vals)]
+    pos = np.unique(pos)
+    lo, hi = pos[:-1], pos[1:]
+    mid = (lo + hi) / 2.0  # exact in double
+    got = oracle.rn16(mid).view(np.uint16)
+    lo_bits = lo.astype(np.float16).view(np.uint16)
+    hi_bits = hi.astype(np.float16).view(np.uint16)
+    want = np.where(lo_bits % 2 == 0, lo_bits, hi_bits)
+    assert np.array_equal(got, want)
+    # a hair either side of the midpoint goes to the nearer neighbour
+    below = np.nextafter(mid, -np.inf)
+    above = np.nextafter(mid, np.inf)
+    assert np.array_equal(oracle.rn16(below).view(np.uint16), lo_bits)
+    assert np.array_equal(oracle.rn16(above).view(np.uint16), hi_bits)
+
+
+def test_rn16_range_edges():
+    bits = lambda v: int(oracle.rn16(np.array([v])).view(np.uint16)[0])
+    assert bits(65519.99) == 0x7BFF          # rounds down to 65504
+    assert bits(65520.0) == 0x7C00           # tie goes to 2^16 = inf
+    assert bits(-65520.0) == 0xFC00
+    assert bits(2.0 ** -25) == 0x0000        # tie between 0 and 2^-24 -> 0
+    assert bits(3 * 2.0 ** -25) == 0x0002    # tie between 1 and 2 quanta -> 2
+    assert bits(2.0 ** -24) == 0x0001
+    assert bits(-0.0) == 0x8000
+    assert bits(np.inf) == 0x7C00
+
+
+# ----------------------------------------------------------- LayerNorm ----
+
+@pytest.mark.parametrize("width", [192, 384])
+def test_ln_constant_rows_map_to_zero(width):
+    consts = np.array([0.0, 1.0, -3.5, 1000.0, -65504.0, 2.0 ** -20], dtype=np.float16)
+    x = np.repeat(consts[:, None], width, axis=1)
+    y = oracle.ln(x, EPS).astype(np.float64)
+    assert (y == 0.0).all()
+
+
+@pytest.mark.parametrize("width", [192, 384, 7])
+def test_ln_moments_closed_form(width):
+    rng = np.random.default_rng(width)
+    for _ in range(20):
+        x = rng.normal(rng.uniform(-4, 4), rng.uniform(0.01, 3.0), width)
+        y = oracle.ln_row_f64(x, EPS)
+        var = np.var(x)  # population variance
+        assert abs(y.mean()) < 1e-13
+        assert np.mean(y * y) == pytest.approx(var / (var + EPS), rel=1e-12)
+
+
+def test_ln_alternating_row_is_plus_minus_one():
+    x = np.tile(np.array([1.0, -1.0], dtype=np.float16), 96)[None, :]
+    y = oracle.ln(x, EPS).astype(np.float64)
+    # unrounded value is +-1/sqrt(1 + eps), which is within half an ulp of 1
+    assert np.array_equal(y[0], np.tile([1.0, -1.0], 96))
+    y64 = oracle.ln_f64(x, EPS)
+    assert y64[0, 0] == pytest.approx(1.0 / np.sqrt(1.0 + EPS), rel=1e-15)
+
+
+def test_ln_shift_invariance_on_integer_rows():
+    rng = np.random.default_rng(3)
+    x = rng.integers(-50, 50, (16, 192)).astype(np.float16)
+    for k in (-100, 7, 512):
+        assert np.array_equal(oracle.ln(x, EPS).view(np.uint16),
+                              oracle.ln((x.astype(np.float64) + k).astype(np.float16), EPS).view(np.uint16))
+
+
+@pytest.mark.parametrize("width", [192, 384])
+def test_ln_matches_torch_float64_layer_norm(width):
+    x = synth.ln_input(512, width, seed=21).numpy()
+    ours = oracle.ln_f64(x, EPS)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x.astype(np.float64)), (width,),
+                                         eps=EPS).numpy()
+    assert np.max(np.abs(ours - ref)) < 1e-12
+    assert np.array_equal(oracle.ln(x, EPS).view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+# ------------------------------------------------- residual add + LN ----
+
+def test_residual_sum_is_fp16_of_fp32_sum():
+    """numpy adds float16 arrays by widening to float32, adding and rounding
+    back: the page's fp16(fp32 a + fp32 b), computed by someone else."""
+    a = np.repeat(_all_f16(), 96)
+    rng = np.random.default_rng(5)
+    b = rng.permutation(np.repeat(_all_f16(), 96))
+    finite = np.isfinite(a.astype(np.float64)) & np.isfinite(b.astype(np.float64))
+    a, b = a[finite], b[finite]
+    n = (a.size // 192) * 192
+    a, b = a[:n].reshape(-1, 192), b[:n].reshape(-1, 192)
+    r, _ = oracle.residual_add_ln(a, b, EPS)
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = (a + b)
+    assert np.array_equal(r.view(np.uint16), want.view(np.uint16))
+
+
+def test_residual_ln_is_taken_after_the_fp16_rounding():
+    a, b = synth.residual_branch(576, 192, seed=0)
+    a, b = a.numpy(), b.numpy()
+    r, y = oracle.residual_add_ln(a, b, EPS)
+    assert np.array_equal(y.view(np.uint16), oracle.ln(r, EPS).view(np.uint16))
+    # LN of the unrounded sum differs somewhere, so the check above has teeth
+    exact = a.astype(np.float64) + b.astype(np.float64)
+    unrounded = torch.nn.functional.layer_norm(torch.from_numpy(exact), (192,), eps=EPS).numpy()
+    assert not np.array_equal(unrounded.astype(np.float16).view(np.uint16), y.view(np.uint16))
+
+
+# ---------------------------------------------------------- index map ----
+
+def brute_force_index(grid, win, shift, padded, flags):
+    """Sort-based construction, independent of the oracle's scatter: list
+    every padded cell with its (window, in-window) key, sort, read sources."""
+    Z, H, W = grid
+    P = padded
+    cells = []
+    for z, h, w in itertools.product(range(P[0]), range(P[1]), range(P[2])):
+        key = (z // win[0], h // win[1], w // win[2], z % win[0], h % win[1], w % win[2])
+        if flags == 0:
+            if z < Z and h < H and w < W:
+                s = (((z + shift[0]) % Z) * H + (h + shift[1]) % H) * W + (w + shift[2]) % W
+            else:
+                s = -1
+        else:
+            zs, hs, ws = (z + shift[0]) % P[0], (h + shift[1]) % P[1], (w + shift[2]) % P[2]
+            s = (zs * H + hs) * W + ws if (zs < Z and hs < H and ws < W) else -1
+        cells.append((key, s))
+    cells.sort()
+    return np.array([s for _, s in cells], dtype=np.int32)
+
+
+def test_index_map_worked_entries():
+    for name, c in window_index_cases().items():
+        m = oracle.build_window_index(c["grid"], c["win"], c["shift"], c["padded"], c["flags"])
+        assert m.size == c["n_idx"], name
+        assert int((m == -1).sum()) == c["n_pads"], name
+        for dst, src in c["entries"]:
+            assert m[dst] == src, (name, dst, m[dst], src)
+
+
+BRUTE_CASES = [
+    ((2, 12, 24), (2, 6, 12), (1, 3, 6), None, 0),
+    ((3, 11, 20), (2, 6, 12), (1, 3, 6), None, 0),
+    ((3, 11, 20), (2, 6, 12), (1, 3, 6), None, 1),
+    ((2, 6, 18), (2, 6, 12), (1, 3, 6), (2, 6, 18), 0),
+    ((3, 5, 7), (2, 2, 3), (-1, 2, -3), None, 0),
+    ((3, 5, 7), (2, 2, 3), (4, -7, 10), (5, 5, 8), 1),
+    ((1, 1, 1), (1, 1, 1), (0, 0, 0), None, 0),
+    ((4, 13, 9), (2, 6, 12), (0, 0, 0), (4, 18, 9), 0),
+]
+
+
+@pytest.mark.parametrize("grid,win,shift,padded,flags", BRUTE_CASES)
+def test_index_map_matches_brute_force(grid, win, shift, padded, flags):
+    P = padded or tuple(-(-g // w) * w for g, w in zip(grid, win))
+    want = brute_force_index(grid, win, shift, P, flags)
+    got = oracle.build_window_index(grid, win, shift, padded, flags)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("stage,padded", [
+    (synth.STAGE_192, None), (synth.STAGE_384, synth.STAGE_384.padded),
+    (synth.STAGE_384, (4, 96, 96)), (synth.TINY_PADDED, None)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_index_map_is_permutation_plus_pads(stage, padded, flags):
+    m = oracle.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, padded, flags)
+    P = padded or tuple(-(-g // w) * w for g, w in zip(stage.grid, synth.WINDOW))
+    assert m.size == P[0] * P[1] * P[2] == oracle.window_index_count(stage.grid, synth.WINDOW, padded)
+    real = m[m >= 0]
+    assert ((m >= -1) & (m < stage.tokens)).all()
+    assert real.size == stage.tokens
+    assert np.array_equal(np.sort(real), np.arange(stage.tokens, dtype=np.int32))
+    assert int((m == -1).sum()) == m.size - stage.tokens
+
+
+def test_index_map_rejects_bad_extents():
+    with pytest.raises(ValueError):
+        oracle.build_window_index((2, 12, 24), (2, 6, 12), (1, 3, 6), (2, 11, 24))
+    with pytest.raises(ValueError):
+        oracle.build_window_index((2, 12, 24), (0, 6, 12), (1, 3, 6))
+
+
+# ------------------------------------------------------------- gather ----
+
+def _iota_rows(n, width):
+    """Row r carries r in its first two elements' bit patterns; the rest are
+    random bits, so any row mix-up or partial copy shows."""
+    rng = np.random.default_rng(n)
+    bits = rng.integers(0, 65536, (n, width), dtype=np.uint32).astype(np.uint16)
+    r = np.arange(n, dtype=np.uint32)
+    bits[:, 0] = (r & 0xFFFF).astype(np.uint16)
+    bits[:, 1] = (r >> 16).astype(np.uint16)
+    return bits.view(np.float16)
+
+
+def test_gather_one_hot_probe():
+    src = _iota_rows(1000, 192)
+    idx = synth.random_index(3000, 1000, 0.2, seed=9).numpy()
+    idx[5] = 1000      # out of range: zero row, counted
+    idx[6] = -7        # below -1: zero row, counted
+    dst, bad = oracle.window_gather(src, idx)
+    assert bad == 2
+    b = dst.view(np.uint16)
+    for d in range(idx.size):
+        if 0 <= idx[d] < 1000:
+            assert int(b[d, 0]) | (int(b[d, 1]) << 16) == idx[d]
+            assert np.array_equal(b[d], src.view(np.uint16)[idx[d]])
+        else:
+            assert not b[d].any()
+
+
+def test_gather_window_map_places_tokens():
+    st = synth.TINY_PADDED
+    src = _iota_rows(st.tokens, 16)
+    m = oracle.build_window_index(st.grid, synth.WINDOW, synth.SHIFT)
+    dst, bad = oracle.window_gather(src, m)
+    assert bad == 0
+    b = dst.view(np.uint16)
+    decoded = b[:, 0].astype(np.int64) | (b[:, 1].astype(np.int64) << 16)
+    assert np.array_equal(decoded[m >= 0], m[m >= 0])
+    assert not b[m < 0].any()
+
+
+def test_norm_gather_is_ln_then_gather():
+    st = synth.TINY_PADDED
+    src = synth.gather_source(st.tokens, 192, seed=3).numpy()
+    m = oracle.build_window_index(st.grid, synth.WINDOW, synth.SHIFT)
+    fused, bad = oracle.norm_gather(src, m, EPS)
+    assert bad == 0
+    two_step, _ = oracle.window_gather(oracle.ln(src, EPS), m)
+    assert np.array_equal(fused.view(np.uint16), two_step.view(np.uint16))
+
+
+def test_gather_empty():
+    dst, bad = oracle.window_gather(np.zeros((4, 8), np.float16), np.zeros(0, np.int32))
+    assert dst.shape == (0, 8) and bad == 0
+
+
+# --------------------------------------------------------------- GELU ----
+
+def _torch_gelu64(t):
+    return torch.nn.functional.gelu(torch.from_numpy(np.asarray(t, np.float64)),
+                                    approximate="tanh").numpy()
+
+
+def test_gelu_f32_matches_torch_float64():
+    x, b = synth.gelu_input(64, 768, torch.float32, seed=4)
+    x, b = x.numpy(), b.numpy()
+    y, y64 = oracle.bias_gelu_tanh(x, b)
+    t = x + b[None, :]  # numpy float32 add: one binary32 rounding
+    ref = _torch_gelu64(t)
+    assert np.max(np.abs(y64 - ref) / np.maximum(np.abs(ref), 1e-300)) < 1e-13
+    assert np.array_equal(y, ref.astype(np.float32))
+
+
+def test_gelu_tiny_page_input():
+    rows, bias = gelu_tiny_input()
+    x = np.array(rows, dtype=np.float32)
+    b = np.array(bias, dtype=np.float32)
+    _, y64 = oracle.bias_gelu_tanh(x, b)
+    ref = _torch_gelu64(x + b[None, :])
+    assert np.allclose(y64, ref, rtol=1e-14, atol=0)
+    # the bias is indexed by column: a row-indexed bias would differ here
+    wrong = _torch_gelu64(x + b[: x.shape[0], None])
+    assert not np.allclose(y64, wrong)
+
+
+def test_gelu_closed_forms():
+    t = np.array([[0.0, 0.5, 1.0, 2.5, 6.0, 20.0]], dtype=np.float32)
+    zero = np.zeros(t.shape[1], np.float32)
+    _, gp = oracle.bias_gelu_tanh(t, zero)
+    _, gm = oracle.bias_gelu_tanh(-t, zero)
+    assert gp[0, 0] == 0.0
+    # tanh is odd, so gelu(t) - gelu(-t) = t exactly in real arithmetic
+    assert np.allclose(gp - gm, t.astype(np.float64), rtol=1e-15, atol=1e-15)
+    assert gp[0, -1] == pytest.approx(20.0, rel=1e-15)
+    # the tanh form, not the erf form: they differ by ~1.5e-4 at t = 1
+    erf_gelu_1 = 0.5 * (1.0 + torch.erf(torch.tensor(1.0, dtype=torch.float64) / np.sqrt(2.0))).item()
+    assert abs(gp[0, 2] - erf_gelu_1) > 1e-4
+
+
+def test_gelu_f16_rounding_point():
+    x, b = synth.gelu_input(48, 1536, torch.float16, seed=4)
+    x, b = x.numpy(), b.numpy()
+    y, y64 = oracle.bias_gelu_tanh(x, b)
+    t16 = x + b[None, :]  # numpy float16 add: fp16(fp32 x + fp32 b)
+    ref = _torch_gelu64(t16.astype(np.float64))
+    assert np.max(np.abs(y64 - ref) / np.maximum(np.abs(ref), 1e-300)) < 1e-13
+    assert np.array_equal(y.view(np.uint16), ref.astype(np.float16).view(np.uint16))
