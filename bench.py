@@ -1,0 +1,540 @@
+#!/usr/bin/env python3
+"""Benchmark of the shifted-window block-glue hot path on GB300.
+
+One step = one pass of every kernel of the path over the Pangu-Weather
+stage shapes, ten launches:
+  ln_fwd, residual_add_ln_fwd, window_gather, norm_gather at
+      C=192: 131040 tokens (8x91x180), 138240 windowed rows (8x96x180)
+      C=384:  32760 tokens (4x91x90),   34560 windowed rows (4x96x90)
+  bias_gelu_tanh fp32 [131040, 768] and fp16 [32760, 1536]
+Window (2,6,12), shift (1,3,6).  Inputs are seeded synthetic tensors.
+
+Metric: effective HBM GB/s (algorithmic bytes: each input read once, each
+output written once, plus the index array) and ms per call per kernel.
+Each kernel is timed with CUDA events on the stream it runs on; the L2 is
+flushed before every launch (write a buffer of 2x L2, then read another of
+2x L2), so inputs come from HBM and no dirty lines are left behind.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+replicas, no collective on the data path); the line reports the sum of the
+ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from window_gather_swin_gb300 import synth  # noqa: E402
+
+METRIC = "effective HBM GB/s and ms/call per fused kernel at [131040,192]/[32760,384]"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+EPS = 1e-5
+CPU_SAMPLE_FRACTION = 0.25
+
+
+# ------------------------------------------------------------ workload ----
+
+class Call:
+    """One kernel invocation of the step with its inputs, outputs and bytes."""
+
+    def __init__(self, name, workload, nbytes, inputs, outputs, run, oracle_run, rows):
+        self.name = name
+        self.workload = workload
+        self.bytes = int(nbytes)
+        self.inputs = inputs        # {key: cpu tensor}
+        self.outputs = outputs      # {key: (shape, dtype)}
+        self.run = run              # run(dev_inputs, dev_outputs)
+        self.oracle_run = oracle_run  # oracle_run(fraction) -> (seconds, algorithmic bytes)
+        self.rows = rows
+
+    @property
+    def label(self):
+        return f"{self.name} {self.workload}"
+
+
+def build_calls():
+    import window_gather_swin_gb300 as wgs
+    calls = []
+    for st in (synth.STAGE_192, synth.STAGE_384):
+        n, c = st.tokens, st.width
+        x = synth.ln_input(n, c, seed=1)
+        calls.append(Call(
+            "ln_fwd", f"[{n},{c}]", 4 * n * c, {"x": x}, {"y": ((n, c), torch.float16)},
+            lambda i, o: wgs.ln_fwd(i["x"], EPS, out=o["y"]),
+            _oracle_rows(lambda f, x=x, n=n: _t(lambda: _orc().ln(x[: _k(n, f)].numpy(), EPS)),
+                         lambda f, n=n, c=c: 4 * _k(n, f) * c), n))
+        a, b = synth.residual_branch(n, c, seed=2)
+        calls.append(Call(
+            "residual_add_ln_fwd", f"[{n},{c}]", 8 * n * c, {"a": a, "b": b},
+            {"r": ((n, c), torch.float16), "y": ((n, c), torch.float16)},
+            lambda i, o: wgs.residual_add_ln_fwd(i["a"], i["b"], EPS, residual_out=o["r"], out=o["y"]),
+            _oracle_rows(lambda f, a=a, b=b, n=n: _t(lambda: _orc().residual_add_ln(
+                a[: _k(n, f)].numpy(), b[: _k(n, f)].numpy(), EPS)),
+                lambda f, n=n, c=c: 8 * _k(n, f) * c), n))
+        src = synth.gather_source(n, c, seed=3)
+        idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+        m = idx.numel()
+        gbytes = 2 * c * n + 2 * c * m + 4 * m
+        for name, fn in (("window_gather", "g"), ("norm_gather", "n")):
+            if fn == "g":
+                run = lambda i, o: wgs.window_gather(i["src"], i["idx"], out=o["dst"])
+                orc = lambda f, src=src, idx=idx, m=m: _t(lambda: _orc().window_gather(
+                    src.numpy(), idx[: _k(m, f)].numpy()))
+            else:
+                run = lambda i, o: wgs.norm_gather(i["src"], i["idx"], EPS, out=o["dst"])
+                orc = lambda f, src=src, idx=idx, m=m: _t(lambda: _orc().norm_gather(
+                    src.numpy(), idx[: _k(m, f)].numpy(), EPS))
+            calls.append(Call(
+                name, f"[{n},{c}]->{m}", gbytes, {"src": src, "idx": idx},
+                {"dst": ((m, c), torch.float16)}, run,
+                _oracle_rows(orc, lambda f, n=n, m=m, c=c: _k(m, f) / m * (2 * c * n) + _k(m, f) * (2 * c + 4)),
+                m))
+    for (rows, width), dt, seed in ((synth.GELU_F32_SHAPE, torch.float32, 4),
+                                    (synth.GELU_F16_SHAPE, torch.float16, 4)):
+        x, b = synth.gelu_input(rows, width, dt, seed=seed)
+        esz = 4 if dt == torch.float32 else 2
+        calls.append(Call(
+            "bias_gelu_tanh", f"{'fp32' if esz == 4 else 'fp16'} [{rows},{width}]",
+            2 * rows * width * esz + width * esz, {"x": x, "bias": b},
+            {"y": ((rows, width), dt)},
+            lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]),
+            _oracle_rows(lambda f, x=x, b=b, rows=rows: _t(lambda: _orc().bias_gelu_tanh(
+                x[: _k(rows, f)].numpy(), b.numpy(), want_f64=False)),
+                lambda f, rows=rows, width=width, esz=esz: 2 * _k(rows, f) * width * esz + width * esz),
+            rows))
+    return calls
+
+
+def _k(n, f):
+    return max(1, int(n * f))
+
+
+def _t(fn):
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
+def _oracle_rows(timer, nbytes):
+    return lambda f: (timer(f), nbytes(f))
+
+
+def _orc():
+    # The oracle is test infrastructure; only the CPU-baseline and the
+    # reference arm of this benchmark execute it.
+    import oracle
+    return oracle
+
+
+# ---------------------------------------------------------------- util ----
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic():
+    """dram bytes per launch from ncu captures, keyed by kernel label.  Each
+    line of profiles/ncu_traffic.txt is `label | sources digest | bytes`; a
+    figure counts only while the kernel sources still hash to its digest."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    digest = sources_digest()
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line.count("|") != 2:
+                continue
+            label, sha, nbytes = (p.strip() for p in line.split("|"))
+            if sha == digest:
+                out[label] = float(nbytes)
+    return out
+
+
+def sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for d in (os.path.join(ROOT, "window_gather_swin_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for name in sorted(os.listdir(d)):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str, interval_ms: int = 50):
+        self.index = index
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        deadline = time.time() + 3.0
+        while not self.lines and time.time() < deadline:  # first sample is in
+            time.sleep(0.01)
+        self.mark = len(self.lines)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(self.interval_ms / 1000.0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l.split(",") for _, l in self.lines[max(self.mark - 1, 0):]]
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if _num(r[1])]
+        mx = [float(r[2]) for r in rows if _num(r[2])]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _num(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ------------------------------------------------------------ our arm ----
+
+def cpu_baseline(calls):
+    """The oracle, as it stands, single-threaded, on the first quarter of the
+    rows of every call of one step."""
+    secs = nbytes = 0.0
+    for c in calls:
+        s, b = c.oracle_run(CPU_SAMPLE_FRACTION)
+        secs += s
+        nbytes += b
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {CPU_SAMPLE_FRACTION:g} of the rows of each of the {len(calls)} calls of "
+                      f"one step ({nbytes / 1e6:.1f} MB algorithmic, {secs:.2f} s)"}
+
+
+def run_ours(args, rank, world, local):
+    import window_gather_swin_gb300 as wgs  # noqa: F401  (loads libwgs.so)
+    from window_gather_swin_gb300 import _capi
+    _capi.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    calls = build_calls()
+    if args.only:
+        calls = [c for c in calls if args.only in c.label]
+        if not calls:
+            raise SystemExit(f"--only {args.only!r} matches no call")
+    dev_in = [{k: v.to(dev) for k, v in c.inputs.items()} for c in calls]
+    dev_out = [{k: torch.empty(s, dtype=d, device=dev) for k, (s, d) in c.outputs.items()}
+               for c in calls]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20)
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, out=sink)
+
+    stream = torch.cuda.current_stream(dev)
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        for c, i, o in zip(calls, dev_in, dev_out):
+            flush()
+            c.run(i, o)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(K)]
+    region = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    sampler = ClockSampler(smi_id(dev))
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    region[0].record(stream)
+    for s in range(K):
+        for j, (c, i, o) in enumerate(zip(calls, dev_in, dev_out)):
+            flush()
+            ev[s][j][0].record(stream)
+            c.run(i, o)
+            ev[s][j][1].record(stream)
+    region[1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    barrier(world)
+    clocks = sampler.stop()
+
+    per = [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(K)] for j in range(len(calls))]
+    kernel_ms_total = sum(sum(p) for p in per)
+    region_ms = region[0].elapsed_time(region[1])
+    step_bytes = sum(c.bytes for c in calls)
+
+    max_kernel_ms = reduce_max(kernel_ms_total, world, dev)
+    all_bytes = reduce_sum(step_bytes * K, world, dev)
+    value = all_bytes / (max_kernel_ms / 1e3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+
+    kernels = []
+    for c, p in zip(calls, per):
+        med = statistics.median(p)
+        mean = statistics.fmean(p)
+        q = sorted(p)
+        gbs = c.bytes / (mean / 1e3) / 1e9
+        kernels.append({"kernel": c.name, "workload": c.workload, "bytes": c.bytes,
+                        "ms_median": round(med, 5), "ms_mean": round(mean, 5),
+                        "ms_min": round(q[0], 5), "ms_p90": round(q[int(0.9 * (len(q) - 1))], 5),
+                        "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                        "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)})
+    dom = max(range(len(calls)), key=lambda j: sum(per[j]))
+    traffic = ncu_traffic().get(calls[dom].label)
+    roofline = {"bound": "hbm", "kernel": calls[dom].label,
+                "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(kernels[dom]["gbs"] / peak, 4), "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes": calls[dom].bytes}
+
+    e2e = None if args.no_e2e else run_e2e(calls, dev, args, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(max_kernel_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "storage_dtype": "fp16 rows (LN, gathers, fp16 GELU), fp32 (fp32 GELU)",
+        "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
+        "config": {"workload": "block-glue hot path, both stages: ln, residual_add_ln, "
+                               "window_gather, norm_gather at [131040,192]->138240 and "
+                               "[32760,384]->34560; bias_gelu fp32 [131040,768], fp16 [32760,1536]",
+                   "window": list(synth.WINDOW), "shift": list(synth.SHIFT),
+                   "launches_per_step": len(calls),
+                   "l2": "flushed before every launch (write 2xL2, read 2xL2); flush outside the "
+                         "kernel events",
+                   "timing": "CUDA events around each launch on its stream; value = all ranks' "
+                             "algorithmic bytes / slowest rank's summed kernel time",
+                   "parallelism": f"replicas x{world}"},
+        "region_ms_per_step_with_flush": round(region_ms / K, 5),
+        "wall_s": round(wall, 3),
+        "kernels": kernels,
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu_launches": K * len(calls),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(calls)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def smi_id(dev):
+    """nvidia-smi --id for a torch device: its UUID when torch reports one."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    return str(dev.index)
+
+
+def run_e2e(calls, dev, args, world):
+    """Same metric through the public API from pinned HOST buffers: every
+    step copies each call's inputs host->device, runs it, and copies its
+    outputs device->host, all inside the timed region."""
+    host_in = [{k: v.pin_memory() for k, v in c.inputs.items()} for c in calls]
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in c.inputs.items()} for c in calls]
+    dev_out = [{k: torch.empty(s, dtype=d, device=dev) for k, (s, d) in c.outputs.items()}
+               for c in calls]
+    host_out = [{k: torch.empty(s, dtype=d, pin_memory=True) for k, (s, d) in c.outputs.items()}
+                for c in calls]
+    h2d = sum(v.numel() * v.element_size() for d in host_in for v in d.values())
+    d2h = sum(v.numel() * v.element_size() for d in host_out for v in d.values())
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for c, hi, di, do, ho in zip(calls, host_in, dev_in, dev_out, host_out):
+            for k in hi:
+                di[k].copy_(hi[k], non_blocking=True)
+            c.run(di, do)
+            for k in do:
+                ho[k].copy_(do[k], non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(a.elapsed_time(b), world, dev)
+    total = reduce_sum(sum(c.bytes for c in calls) * steps, world, dev)
+    return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+# ------------------------------------------------------- reference arm ----
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, as the reference arm: each step runs
+    every call of the step on a bounded sample of its rows."""
+    if world > 1:
+        init_dist(world, "gloo")
+        if rank != 0:
+            torch.distributed.destroy_process_group()
+            return
+    calls = build_calls()
+    # size the per-step sample so the whole run stays within ~2 minutes
+    probe = 1.0 / 1024
+    probe_s = sum(c.oracle_run(probe)[0] for c in calls)
+    full_step_s = probe_s / probe
+    budget_s = 120.0
+    frac = budget_s / (full_step_s * (args.steps + args.warmup))
+    frac = max(1.0 / 16384, min(1.0 / 16, frac))
+    for _ in range(args.warmup):
+        for c in calls:
+            c.oracle_run(frac)
+    secs = nbytes = 0.0
+    for _ in range(args.steps):
+        for c in calls:
+            s, b = c.oracle_run(frac)
+            secs += s
+            nbytes += b
+    value = nbytes / secs / 1e9
+    sample = (f"first {frac:.3g} of the rows of each of the {len(calls)} calls per step "
+              f"({nbytes / args.steps / 1e6:.2f} MB algorithmic per step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
+        "config": {"workload": "block-glue hot path, both stages (oracle on a row sample)",
+                   "parallelism": "rank 0 only"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--only", default=None,
+                   help="time only the calls whose label contains this text (profiling aid)")
+    args = p.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        p.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            p.error(f"--gpus {args.gpus} needs torchrun with {args.gpus} processes")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * wgs.h -- C ABI of the GB300 (sm_103a) block-glue kernels of a
+ * shifted-window (Swin / Pangu-Weather style) transformer block.
+ *
+ * Sources (page title, section):
+ *   [P1] "BW1000 gfx936 Pangu-Weather inference profiling"
+ *        (l189.com news 2144533)
+ *        s3  fixed-width LayerNorm, affine folded into the next Linear
+ *        s4  fused residual add + norm, keeping the FP16 rounding point
+ *        s5  window gather with a precomputed INT32 index protocol, and the
+ *            fused norm-then-gather
+ *   [P3] "PyTorch + HIP fused bias + GELU on Hygon DCU"
+ *        (forum.sourcefind.cn)
+ *        s3  math semantics: tanh-approximate GELU of input + bias
+ *        s6  interface checks: clear errors for bad inputs, empty input
+ *            launches nothing, work goes on the caller's stream, launch
+ *            status is checked
+ *
+ * Conventions shared by every device entry point
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     row-major and dense (row r starts at r * width elements).
+ *   - The caller owns every buffer.  The library allocates no device
+ *     memory, never synchronises the stream and never touches the default
+ *     stream unless the caller passes it (stream 0).
+ *   - Work is enqueued on `stream`; the call returns once it is enqueued.
+ *   - Arguments are checked before anything is launched; a failed check
+ *     returns a status and launches nothing.  A launch failure reported by
+ *     the runtime returns WGS_ERR_LAUNCH.
+ *   - A call with zero rows (or zero indices) returns WGS_OK and launches
+ *     nothing; its pointers may then be NULL.
+ *   - fp16 is IEEE binary16; "fp16(v)" below is round-to-nearest-even.
+ *   - The kernels run only on compute capability 10.3 (sm_103a); on any
+ *     other device the entry points return WGS_ERR_ARCH.
+ *   - Calls are thread-safe; the only shared state is the per-device index
+ *     error word read by wgs_check_error().
+ */
+#ifndef WGS_H
+#define WGS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WGS_ABI_VERSION 1
+
+typedef enum {
+    WGS_OK = 0,
+    WGS_ERR_NULL = 1,    /* a required pointer is NULL                      */
+    WGS_ERR_SHAPE = 2,   /* negative size, or sizes inconsistent            */
+    WGS_ERR_WIDTH = 3,   /* width not supported by this entry point         */
+    WGS_ERR_ALIGN = 4,   /* a pointer is not aligned as required            */
+    WGS_ERR_DTYPE = 5,   /* unknown dtype code                              */
+    WGS_ERR_ARCH = 6,    /* current device is not compute capability 10.3   */
+    WGS_ERR_LAUNCH = 7,  /* the CUDA runtime rejected the launch            */
+    WGS_ERR_INDEX = 8,   /* a gather index was outside [-1, n_src)          */
+    WGS_ERR_ALIAS = 9,   /* buffers overlap in a way the operation forbids  */
+    WGS_ERR_CUDA = 10    /* another CUDA runtime call failed                */
+} wgs_status;
+
+typedef enum { WGS_F32 = 0, WGS_F16 = 1 } wgs_dtype;
+
+/* Index-map construction order (wgs_build_window_index). */
+#define WGS_SHIFT_THEN_PAD 0
+#define WGS_PAD_THEN_SHIFT 1
+
+/* Human-readable name of a status; never NULL. */
+const char *wgs_status_string(wgs_status s);
+
+/* WGS_ABI_VERSION of the built library. */
+int32_t wgs_abi_version(void);
+
+/* ------------------------------------------------------------------ */
+/* ln_fwd -- LayerNorm without affine                          [P1 s3] */
+/* ------------------------------------------------------------------ */
+/* For each of `rows` rows of `width` fp16 values:
+ *     mean = sum(x) / width,  var = sum((x - mean)^2) / width   (FP32)
+ *     y    = fp16((x - mean) / sqrt(var + eps))
+ * The affine scale and shift are not applied: the model folds them into
+ * the following Linear at load time.
+ *   x, y   fp16 [rows, width], 16-byte aligned.  y == x (in place) is
+ *          allowed; any other overlap returns WGS_ERR_ALIAS.
+ *   width  192 or 384 only (else WGS_ERR_WIDTH): the model's two hidden
+ *          widths; there is no generic fallback.
+ *   eps    added to the variance inside the square root (1e-5 in the model). */
+wgs_status ln_fwd(const void *x, void *y, int64_t rows, int32_t width, float eps,
+                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* residual_add_ln_fwd -- fused residual add + LayerNorm       [P1 s4] */
+/* ------------------------------------------------------------------ */
+/*     residual_out = fp16(fp32(residual) + fp32(branch))   (written out)
+ *     y            = LN(residual_out)                       (as ln_fwd)
+ * The normalisation starts from the ROUNDED fp16 residual_out, the same
+ * rounding point as a separate add followed by a separate LayerNorm.
+ *   residual, branch, residual_out, y  fp16 [rows, width], 16-byte aligned.
+ *   residual_out may equal residual or branch; y may equal residual or
+ *   branch; residual_out and y must be distinct; partial overlaps return
+ *   WGS_ERR_ALIAS.
+ *   width  192 or 384 only. */
+wgs_status residual_add_ln_fwd(const void *residual, const void *branch, void *residual_out,
+                               void *y, int64_t rows, int32_t width, float eps,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* window_gather -- shifted-window token gather               [P1 s5] */
+/* ------------------------------------------------------------------ */
+/* For d in [0, n_idx):
+ *     dst[d] = src[idx[d]]   if 0 <= idx[d] < n_src   (bit-exact row copy)
+ *     dst[d] = 0             if idx[d] == -1           (all-zero pad row)
+ * so padding needs no zero-filled tensor.  An index outside [-1, n_src) is
+ * a caller error: its row is written as zeros and the device error word is
+ * set (see wgs_check_error); nothing faults.
+ *   src  fp16 [n_src, width], dst fp16 [n_idx, width], both 16-byte
+ *        aligned; they must not overlap (WGS_ERR_ALIAS).
+ *   idx  int32 [n_idx], 4-byte aligned, device memory.  Usually built once
+ *        per window shape with wgs_build_window_index and copied to the
+ *        device.
+ *   width  any multiple of 8 (rows are whole 16-byte chunks); 192 and 384
+ *          take a specialised path. */
+wgs_status window_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                         int64_t n_idx, int32_t width, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* norm_gather -- fused LayerNorm then window gather          [P1 s5] */
+/* ------------------------------------------------------------------ */
+/*     dst[d] = LN(src[idx[d]])  for a valid index, 0 for idx[d] == -1
+ * The normalised tensor is never materialised: each gathered row is
+ * normalised in registers on its way to dst.  Results equal ln_fwd
+ * followed by window_gather bit for bit.  Buffers, index rules and errors
+ * as window_gather; width 192 or 384 only. */
+wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                       int64_t n_idx, int32_t width, float eps, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* bias_gelu_tanh -- fused bias + tanh-approximate GELU       [P3 s3] */
+/* ------------------------------------------------------------------ */
+/*     t = x + bias[col]   (rounded once to the tensor dtype)
+ *     y = 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3)))
+ * evaluated in FP32 and rounded to the tensor dtype.
+ *   x, y   [rows, width] of `dtype` (WGS_F32 or WGS_F16); y == x allowed,
+ *          other overlaps return WGS_ERR_ALIAS.
+ *   bias   [width] of `dtype`; must not overlap y.
+ *   width  any value >= 1.  A 16-byte vector path runs when width is a
+ *          multiple of 4 (f32) or 8 (f16) and all pointers are 16-byte
+ *          aligned; otherwise a scalar path runs (same results). */
+wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows, int32_t width,
+                          wgs_dtype dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Host-side window index map                                 [P1 s5] */
+/* ------------------------------------------------------------------ */
+/* The page fixes the protocol (INT32 per destination row, >= 0 source
+ * token, -1 zero row, precomputed once per window shape); the
+ * construction below is this library's reading of it:
+ *   - tokens are the row-major flattening of a grid[0] x grid[1] x grid[2]
+ *     (Z, H, W) grid;
+ *   - the padded grid has extents padded[k] >= grid[k]; padded == NULL
+ *     rounds each extent up to a multiple of window[k];
+ *   - windows tile the padded grid from the origin, the last one on an axis
+ *     cut short when the padded extent is not a window multiple;
+ *   - destination rows run window by window (row-major over the window
+ *     grid), then row-major over the cells of each window;
+ *   - WGS_SHIFT_THEN_PAD: a cell (z,h,w) inside the grid reads token
+ *     ((z+s0) mod Z, (h+s1) mod H, (w+s2) mod W) -- a cyclic roll by
+ *     -shift -- and every other cell is -1;
+ *     WGS_PAD_THEN_SHIFT: the roll runs over the padded grid, and a rolled
+ *     position outside the grid is -1.
+ * Host memory only; no CUDA call is made. */
+
+/* Number of destination rows (product of the padded extents), or -1 for
+ * invalid extents (grid or window < 1, padded < grid). */
+int64_t wgs_window_index_count(const int32_t grid[3], const int32_t window[3],
+                               const int32_t *padded);
+
+/* Fill out_host[0 .. count) with the map.  out_len must be at least the
+ * count (else WGS_ERR_SHAPE); the token count must fit in int32. */
+wgs_status wgs_build_window_index(const int32_t grid[3], const int32_t window[3],
+                                  const int32_t shift[3], const int32_t *padded, int32_t flags,
+                                  int32_t *out_host, int64_t out_len);
+
+/* Read and clear the current device's index error word after the work
+ * already queued on `stream` has finished.  This call synchronises
+ * `stream`.  Returns WGS_ERR_INDEX if any gather since the last check met
+ * an index outside [-1, n_src), WGS_OK otherwise.  The word is shared by
+ * every stream of the device. */
+wgs_status wgs_check_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WGS_H */

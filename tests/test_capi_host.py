@@ -1,0 +1,173 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every entry point include/wgs.h declares, the host index-map
+builder equals the oracle's bit for bit, and argument errors come back as
+status codes before anything touches a device.
+
+Every call here with fake device pointers carries at least one error that
+the library rejects during argument checking, so no kernel is ever
+launched on them (on a machine with or without a GPU).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from window_gather_swin_gb300 import _capi, synth
+from window_gather_swin_gb300 import api as wgs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wgs.h")
+
+OK, NULL, SHAPE, WIDTH, ALIGN, DTYPE, ARCH, LAUNCH, INDEX, ALIAS = range(10)
+A = 0x10000000  # fake 16-byte aligned "device" addresses; never dereferenced
+B = 0x20000000
+C = 0x30000000
+D = 0x40000000
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _capi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"ln_fwd", "residual_add_ln_fwd", "window_gather", "norm_gather",
+            "bias_gelu_tanh", "wgs_build_window_index", "wgs_window_index_count",
+            "wgs_check_error", "wgs_status_string", "wgs_abi_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_capi.SIGNATURES), "binding table out of step with wgs.h"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.wgs_abi_version() == 1
+    for s in range(11):
+        assert lib.wgs_status_string(s)
+    assert b"unknown" in lib.wgs_status_string(99)
+
+
+# ------------------------------------------------------- index map (a3) ----
+
+CASES = [
+    (synth.STAGE_192.grid, None, 0), (synth.STAGE_192.grid, None, 1),
+    (synth.STAGE_384.grid, synth.STAGE_384.padded, 0),
+    (synth.STAGE_384.grid, (4, 96, 96), 0), (synth.STAGE_384.grid, synth.STAGE_384.padded, 1),
+    (synth.TINY.grid, None, 0), (synth.TINY_PADDED.grid, None, 0),
+    (synth.TINY_PADDED.grid, None, 1), ((2, 6, 18), (2, 6, 18), 0),
+]
+
+
+@pytest.mark.parametrize("grid,padded,flags", CASES)
+def test_library_index_map_equals_oracle(grid, padded, flags):
+    got = wgs.build_window_index(grid, synth.WINDOW, synth.SHIFT, padded, flags).numpy()
+    want = oracle.build_window_index(grid, synth.WINDOW, synth.SHIFT, padded, flags)
+    assert got.dtype == np.int32
+    assert np.array_equal(got, want)
+    assert wgs.window_index_count(grid, synth.WINDOW, padded) == want.size
+
+
+@pytest.mark.parametrize("shift", [(0, 0, 0), (-1, -3, -6), (9, 100, -250), (1, 3, 6)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_library_index_map_odd_shifts(shift, flags):
+    grid, win = (3, 7, 10), (2, 3, 4)
+    got = wgs.build_window_index(grid, win, shift, None, flags).numpy()
+    want = oracle.build_window_index(grid, win, shift, None, flags)
+    assert np.array_equal(got, want)
+
+
+def test_index_builder_errors(lib):
+    g = (ctypes.c_int32 * 3)(2, 12, 24)
+    w = (ctypes.c_int32 * 3)(2, 6, 12)
+    s = (ctypes.c_int32 * 3)(1, 3, 6)
+    small = (ctypes.c_int32 * 3)(2, 11, 24)
+    bad_w = (ctypes.c_int32 * 3)(0, 6, 12)
+    out = (ctypes.c_int32 * 576)()
+    assert lib.wgs_window_index_count(g, w, None) == 576
+    assert lib.wgs_window_index_count(g, w, small) == -1
+    assert lib.wgs_window_index_count(g, bad_w, None) == -1
+    assert lib.wgs_build_window_index(g, w, s, None, 0, out, 575) == SHAPE
+    assert lib.wgs_build_window_index(g, w, s, None, 2, out, 576) == SHAPE
+    assert lib.wgs_build_window_index(None, w, s, None, 0, out, 576) == NULL
+    assert lib.wgs_build_window_index(g, w, s, None, 0, None, 576) == NULL
+    assert lib.wgs_build_window_index(g, w, s, small, 0, out, 576) == SHAPE
+    assert lib.wgs_build_window_index(g, w, s, None, 0, out, 576) == OK
+
+
+# ------------------------------------------------ argument checking ----
+
+def test_ln_argument_errors(lib):
+    assert lib.ln_fwd(A, B, 10, 100, 1e-5, None) == WIDTH
+    assert lib.ln_fwd(A, B, 10, 191, 1e-5, None) == WIDTH
+    assert lib.ln_fwd(A, B, -1, 192, 1e-5, None) == SHAPE
+    assert lib.ln_fwd(A, B, 2 ** 62, 192, 1e-5, None) == SHAPE
+    assert lib.ln_fwd(None, None, 0, 192, 1e-5, None) == OK      # empty: nothing launched
+    assert lib.ln_fwd(None, B, 10, 192, 1e-5, None) == NULL
+    assert lib.ln_fwd(A + 8, B, 10, 192, 1e-5, None) == ALIGN
+    assert lib.ln_fwd(A, A + 16, 10, 192, 1e-5, None) == ALIAS    # partial overlap
+
+
+def test_residual_add_ln_argument_errors(lib):
+    f = lib.residual_add_ln_fwd
+    assert f(A, B, C, D, 10, 96, 1e-5, None) == WIDTH
+    assert f(A, B, C, D, -3, 384, 1e-5, None) == SHAPE
+    assert f(None, None, None, None, 0, 384, 1e-5, None) == OK
+    assert f(A, None, C, D, 10, 384, 1e-5, None) == NULL
+    assert f(A, B, C + 2, D, 10, 384, 1e-5, None) == ALIGN
+    assert f(A, B, C, C, 10, 384, 1e-5, None) == ALIAS           # residual_out == y
+    assert f(A, B, C, C + 768, 10, 384, 1e-5, None) == ALIAS     # they overlap
+    assert f(A, B, A + 768, D, 10, 384, 1e-5, None) == ALIAS     # shifted in-place
+
+
+def test_gather_argument_errors(lib):
+    for fn, extra in ((lib.window_gather, ()), (lib.norm_gather, (1e-5,))):
+        assert fn(A, B, C, 10, 5, 100, *extra, None) == WIDTH
+        assert fn(A, B, C, -1, 5, 192, *extra, None) == SHAPE
+        assert fn(A, B, C, 10, -5, 192, *extra, None) == SHAPE
+        assert fn(None, None, None, 10, 0, 192, *extra, None) == OK
+        assert fn(A, None, C, 10, 5, 192, *extra, None) == NULL
+        assert fn(None, B, C, 10, 5, 192, *extra, None) == NULL   # n_src > 0 needs src
+        assert fn(A, B + 2, C, 10, 5, 192, *extra, None) == ALIGN
+        assert fn(A, B, C + 4, 10, 5, 192, *extra, None) == ALIGN
+        assert fn(A, B, A + 384, 10, 5, 192, *extra, None) == ALIAS  # dst inside src
+        assert fn(A, C + 16, C, 10, 5, 192, *extra, None) == ALIAS   # idx inside dst
+    assert lib.norm_gather(A, B, C, 10, 5, 64, 1e-5, None) == WIDTH   # LN widths only
+    assert lib.window_gather(A, B, C, 10, 5, 12, None) == WIDTH       # not a 16-byte row
+
+
+def test_gelu_argument_errors(lib):
+    f = lib.bias_gelu_tanh
+    assert f(A, B, C, 10, 768, 7, None) == DTYPE
+    assert f(A, B, C, -1, 768, 0, None) == SHAPE
+    assert f(A, B, C, 10, -2, 0, None) == SHAPE
+    assert f(None, None, None, 0, 768, 0, None) == OK
+    assert f(None, None, None, 10, 0, 1, None) == OK
+    assert f(A, None, C, 10, 768, 0, None) == NULL
+    assert f(A + 2, B, C, 10, 768, 0, None) == ALIGN                # f32 needs 4 bytes
+    assert f(A + 1, B, C, 10, 768, 1, None) == ALIGN                # f16 needs 2 bytes
+    assert f(A, B, A + 4, 10, 768, 0, None) == ALIAS
+    assert f(A, C + 8, C, 10, 768, 0, None) == ALIAS                # bias inside y
+
+
+# ------------------------------------------- Python-side contract checks ----
+
+def test_python_rejects_cpu_and_bad_tensors():
+    import torch
+    x = torch.zeros(4, 192, dtype=torch.float16)
+    with pytest.raises(RuntimeError, match="CUDA"):
+        wgs.ln_fwd(x)
+    with pytest.raises(RuntimeError, match="CUDA"):
+        wgs.bias_gelu_tanh(torch.zeros(2, 3), torch.zeros(3))
+    with pytest.raises(RuntimeError, match="CUDA"):
+        wgs.window_gather(x, torch.zeros(3, dtype=torch.int32))
+    with pytest.raises(RuntimeError):
+        wgs.build_window_index((2, 12, 24), (2, 6, 12), (1, 3, 6), padded=(2, 11, 24))

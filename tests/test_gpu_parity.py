@@ -1,0 +1,353 @@
+"""CUDA path vs the CPU oracle, through the C ABI (via the thin binding), on
+seeded synthetic inputs: the tiny block, ragged and edge sizes, and the
+full-size workloads in the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import window_gather_swin_gb300 as wgs
+from parity import assert_bitwise, check_fp16_near, check_gelu_f32, check_ln
+from window_gather_swin_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-5
+DEV = "cuda:0"
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def window_map(stage, padded="stage", flags=0):
+    p = stage.padded if padded == "stage" else padded
+    return wgs.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, p, flags)
+
+
+def oracle_map(stage, padded="stage", flags=0):
+    p = stage.padded if padded == "stage" else padded
+    return oracle.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, p, flags)
+
+
+# ---------------------------------------------------------- tiny block ----
+
+@pytest.mark.parametrize("stage", [synth.TINY, synth.TINY_PADDED], ids=lambda s: s.name)
+def test_tiny_block_end_to_end(stage):
+    """residual add + LN, then norm-gather through the window map, then the
+    bias + GELU epilogue: the tiny configuration, every output compared."""
+    a, b, x, bias = synth.tiny_block(seed=0, stage=stage)
+    r, y = wgs.residual_add_ln_fwd(a.to(DEV), b.to(DEV), EPS)
+    o_r, o_y = oracle.residual_add_ln(a.numpy(), b.numpy(), EPS)
+    assert_bitwise(np_(r), o_r, "residual_out")
+    check_ln(np_(y), o_y, oracle.ln_f64(o_r, EPS), "ln(residual_out)")
+
+    m = window_map(stage)
+    om = oracle_map(stage)
+    assert np.array_equal(m.numpy(), om)
+    g = wgs.norm_gather(r, m.to(DEV), EPS)
+    og, bad = oracle.norm_gather(o_r, om, EPS)
+    assert bad == 0
+    src64 = oracle.ln_f64(o_r, EPS)
+    want64 = np.where((om >= 0)[:, None], src64[np.maximum(om, 0)], 0.0)
+    check_ln(np_(g), og, want64, "norm_gather")
+    assert_bitwise(np_(g)[om < 0], og[om < 0], "pad rows")
+
+    z = wgs.bias_gelu_tanh(x.to(DEV), bias.to(DEV))
+    _, y64 = oracle.bias_gelu_tanh(x.numpy(), bias.numpy())
+    check_gelu_f32(np_(z), y64, "bias_gelu_tanh f32")
+    wgs.check_error(DEV)
+
+
+# ---------------------------------------------------------- LN family ----
+
+@pytest.mark.parametrize("width", [192, 384])
+@pytest.mark.parametrize("rows", [1, 3, 31, 33, 257, 4097])
+def test_ln_ragged_rows(rows, width):
+    x = synth.ln_input(rows, width, seed=rows)
+    y = wgs.ln_fwd(x.to(DEV), EPS)
+    check_ln(np_(y), oracle.ln(x.numpy(), EPS), oracle.ln_f64(x.numpy(), EPS), f"ln {rows}x{width}")
+
+
+@pytest.mark.parametrize("stage", [synth.STAGE_192, synth.STAGE_384], ids=lambda s: s.name)
+def test_ln_full_size(stage):
+    x = synth.ln_input(stage.tokens, stage.width, seed=1)
+    y = wgs.ln_fwd(x.to(DEV), EPS)
+    st = check_ln(np_(y), oracle.ln(x.numpy(), EPS), oracle.ln_f64(x.numpy(), EPS), "ln full")
+    print("ln", stage.name, st)
+
+
+@pytest.mark.parametrize("stage", [synth.STAGE_192, synth.STAGE_384], ids=lambda s: s.name)
+def test_residual_add_ln_full_size(stage):
+    a, b = synth.residual_branch(stage.tokens, stage.width, seed=2)
+    r, y = wgs.residual_add_ln_fwd(a.to(DEV), b.to(DEV), EPS)
+    o_r, o_y = oracle.residual_add_ln(a.numpy(), b.numpy(), EPS)
+    assert_bitwise(np_(r), o_r, "residual_out")
+    st = check_ln(np_(y), o_y, oracle.ln_f64(o_r, EPS), "add+ln")
+    print("add+ln", stage.name, st)
+
+
+@pytest.mark.parametrize("width", [192, 384])
+def test_residual_add_ln_ragged_and_extremes(width):
+    rows = 37
+    a, b = synth.residual_branch(rows, width, seed=7)
+    a[0] = 60000.0            # overflows to inf after the add: row 0 of y is NaN
+    b[0] = 60000.0
+    a[1] = 3.0                # constant row: y must be exactly zero
+    b[1] = 0.0
+    a[2, ::2] = 2.0 ** -20    # subnormal sums
+    b[2, ::2] = -(2.0 ** -21)
+    r, y = wgs.residual_add_ln_fwd(a.to(DEV), b.to(DEV), EPS)
+    o_r, o_y = oracle.residual_add_ln(a.numpy(), b.numpy(), EPS)
+    assert_bitwise(np_(r), o_r, "residual_out")
+    assert np.isnan(np_(y)[0].astype(np.float32)).all()
+    assert (np_(y)[1].astype(np.float32) == 0).all()
+    check_ln(np_(y)[1:], o_y[1:], oracle.ln_f64(o_r[1:], EPS), "add+ln rows 1..")
+
+
+def test_ln_in_place_and_aliasing():
+    x = synth.ln_input(1000, 192, seed=4).to(DEV)
+    want = wgs.ln_fwd(x, EPS)
+    xi = x.clone()
+    wgs.ln_fwd(xi, EPS, out=xi)
+    assert torch.equal(xi.view(torch.int16), want.view(torch.int16))
+    a, b = synth.residual_branch(500, 384, seed=5)
+    a, b = a.to(DEV), b.to(DEV)
+    r0, y0 = wgs.residual_add_ln_fwd(a, b, EPS)
+    a2 = a.clone()
+    wgs.residual_add_ln_fwd(a2, b, EPS, residual_out=a2)     # residual_out == residual
+    assert torch.equal(a2.view(torch.int16), r0.view(torch.int16))
+
+
+def test_cross_kernel_identities():
+    """norm_gather == window_gather o ln_fwd, and residual_add_ln(a, 0)
+    == (a, ln_fwd(a)), bit for bit: one row-normalise routine serves all."""
+    st = synth.STAGE_384
+    x = synth.gather_source(st.tokens, st.width, seed=3).to(DEV)
+    m = window_map(st).to(DEV)
+    fused = wgs.norm_gather(x, m, EPS)
+    two = wgs.window_gather(wgs.ln_fwd(x, EPS), m)
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    a = synth.ln_input(3001, 192, seed=8).to(DEV)
+    r, y = wgs.residual_add_ln_fwd(a, torch.zeros_like(a), EPS)
+    assert torch.equal(r.view(torch.int16), a.view(torch.int16))
+    assert torch.equal(y.view(torch.int16), wgs.ln_fwd(a, EPS).view(torch.int16))
+
+
+# ------------------------------------------------------------- gathers ----
+
+@pytest.mark.parametrize("stage,padded", [
+    (synth.STAGE_192, "stage"), (synth.STAGE_384, "stage"), (synth.STAGE_384, (4, 96, 96))],
+    ids=["c192", "c384", "c384_full_pad"])
+def test_window_gather_full_size(stage, padded):
+    src = synth.gather_source(stage.tokens, stage.width, seed=3)
+    m = window_map(stage, padded)
+    om = oracle_map(stage, padded)
+    assert np.array_equal(m.numpy(), om)
+    dst = wgs.window_gather(src.to(DEV), m.to(DEV))
+    want, bad = oracle.window_gather(src.numpy(), om)
+    assert bad == 0
+    assert_bitwise(np_(dst), want, "window_gather")
+
+
+@pytest.mark.parametrize("stage", [synth.STAGE_192, synth.STAGE_384], ids=lambda s: s.name)
+def test_norm_gather_full_size(stage):
+    src = synth.gather_source(stage.tokens, stage.width, seed=3)
+    m = window_map(stage)
+    om = oracle_map(stage)
+    dst = wgs.norm_gather(src.to(DEV), m.to(DEV), EPS)
+    want, bad = oracle.norm_gather(src.numpy(), om, EPS)
+    assert bad == 0
+    src64 = oracle.ln_f64(src.numpy(), EPS)
+    want64 = np.where((om >= 0)[:, None], src64[np.maximum(om, 0)], 0.0)
+    g = np_(dst)
+    assert_bitwise(g[om < 0], want[om < 0], "pad rows")
+    st = check_ln(g, want, want64, "norm_gather")
+    print("norm_gather", stage.name, st)
+
+
+def _iota_rows(n, width):
+    rng = np.random.default_rng(n)
+    bits = rng.integers(0, 65536, (n, width), dtype=np.uint32).astype(np.uint16)
+    r = np.arange(n, dtype=np.uint32)
+    bits[:, 0] = (r & 0xFFFF).astype(np.uint16)
+    bits[:, 1] = (r >> 16).astype(np.uint16)
+    return bits.view(np.float16)
+
+
+@pytest.mark.parametrize("width", [8, 64, 192, 384, 520])
+@pytest.mark.parametrize("n_idx", [1, 5, 333, 70001])
+def test_gather_one_hot_probe(width, n_idx):
+    """Every source row carries its own number (and random payload bits,
+    NaN patterns included): each destination row must decode to its index."""
+    n_src = 5000
+    src = _iota_rows(n_src, width)
+    idx = synth.random_index(n_idx, n_src, 0.15, seed=n_idx).numpy()
+    dst = wgs.window_gather(torch.from_numpy(src).to(DEV), torch.from_numpy(idx).to(DEV))
+    want, bad = oracle.window_gather(src, idx)
+    assert bad == 0
+    assert_bitwise(np_(dst), want, f"gather w={width} n={n_idx}")
+
+
+def test_invalid_index_sets_error_word_and_writes_zero_rows():
+    wgs.check_error(DEV)  # start clean
+    src = synth.gather_source(100, 192, seed=1)
+    idx = torch.tensor([0, 99, -1, 100, -2, 2 ** 31 - 1, 5], dtype=torch.int32)
+    for fn in (wgs.window_gather, wgs.norm_gather):
+        dst = fn(src.to(DEV), idx.to(DEV))
+        d = np_(dst).view(np.uint16)
+        assert not d[[2, 3, 4, 5]].any()
+        with pytest.raises(wgs.WgsError, match="WGS_ERR_INDEX"):
+            wgs.check_error(DEV)
+        wgs.check_error(DEV)  # the word was cleared by the read
+    want, bad = oracle.window_gather(src.numpy(), idx.numpy())
+    assert bad == 3
+    assert_bitwise(np_(wgs.window_gather(src.to(DEV), idx.to(DEV))), want, "gather w/ bad idx")
+    with pytest.raises(wgs.WgsError):
+        wgs.check_error(DEV)
+
+
+def test_gather_all_pads_and_empty_source():
+    idx = torch.full((77,), -1, dtype=torch.int32, device=DEV)
+    src = torch.empty((0, 192), dtype=torch.float16, device=DEV)
+    dst = wgs.window_gather(src, idx)
+    assert not np_(dst).view(np.uint16).any()
+    dst = wgs.norm_gather(src, idx)
+    assert not np_(dst).view(np.uint16).any()
+
+
+# ---------------------------------------------------------------- GELU ----
+
+def test_gelu_f32_full_size():
+    x, b = synth.gelu_input(*synth.GELU_F32_SHAPE, torch.float32, seed=4)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    _, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
+    print("gelu f32", check_gelu_f32(np_(y), y64, "gelu f32 full"))
+
+
+def test_gelu_f16_full_size():
+    x, b = synth.gelu_input(*synth.GELU_F16_SHAPE, torch.float16, seed=4)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    o16, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
+    print("gelu f16", check_fp16_near(np_(y), o16, y64, "gelu f16 full"))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("rows,width", [(1, 1), (3, 7), (5, 3), (17, 768), (1025, 1536),
+                                        (33, 1000), (2, 4100)])
+def test_gelu_widths_and_paths(rows, width, dtype):
+    x, b = synth.gelu_input(rows, width, dtype, seed=rows + width)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    o, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
+    if dtype == torch.float32:
+        check_gelu_f32(np_(y), y64, f"gelu {rows}x{width}")
+    else:
+        check_fp16_near(np_(y), o, y64, f"gelu16 {rows}x{width}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+def test_gelu_misaligned_views_take_the_scalar_path(dtype):
+    x, b = synth.gelu_input(65, 769, dtype, seed=3)
+    xd = x.to(DEV).view(-1)[1:1 + 64 * 768].view(64, 768)   # 4 / 2 bytes off a 16-byte line
+    bd = b.to(DEV)[1:]
+    y = wgs.bias_gelu_tanh(xd, bd)
+    o, y64 = oracle.bias_gelu_tanh(np_(xd), np_(bd))
+    if dtype == torch.float32:
+        check_gelu_f32(np_(y), y64, "gelu misaligned")
+    else:
+        check_fp16_near(np_(y), o, y64, "gelu16 misaligned")
+
+
+def test_gelu_special_values():
+    t = torch.tensor([[0.0, -0.0, 1e-30, -1e-30, 3.0e38, -3.0e38, float("inf"), float("-inf"),
+                       float("nan"), -9.5, -12.0, 20.0]], dtype=torch.float32)
+    zero = torch.zeros(t.shape[1])
+    y = np_(wgs.bias_gelu_tanh(t.to(DEV), zero.to(DEV)))
+    _, y64 = oracle.bias_gelu_tanh(t.numpy(), zero.numpy())
+    fin = np.isfinite(y64)
+    check_gelu_f32(y[fin], y64[fin], "gelu specials")
+    assert np.isnan(y[~fin & np.isnan(y64)]).all()
+    assert y[0, 6] == np.inf
+
+
+def test_gelu_page_tiny_input():
+    from golden_io import gelu_tiny_input
+    rows, bias = gelu_tiny_input()
+    x = torch.tensor(rows, dtype=torch.float32)
+    b = torch.tensor(bias, dtype=torch.float32)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    _, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
+    check_gelu_f32(np_(y), y64, "gelu tiny page input")
+
+
+# ------------------------------------------------------- guard bands ----
+
+def _guarded(shape, dtype, fill):
+    n = int(np.prod(shape))
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device=DEV)
+    return buf, buf[pad:pad + n].view(shape), pad
+
+
+def test_outputs_fully_written_and_guards_untouched():
+    """NaN-poisoned outputs inside guard bands: every output element is
+    written, nothing outside the output is touched."""
+    rows = 2049
+    x = synth.ln_input(rows, 384, seed=6).to(DEV)
+    buf, y, pad = _guarded((rows, 384), torch.float16, float("nan"))
+    wgs.ln_fwd(x, EPS, out=y)
+    assert not torch.isnan(y).any()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all()
+
+    st = synth.TINY_PADDED
+    src = synth.gather_source(st.tokens, 192, seed=2).to(DEV)
+    m = window_map(st).to(DEV)
+    buf, dst, pad = _guarded((m.numel(), 192), torch.float16, float("nan"))
+    wgs.norm_gather(src, m, EPS, out=dst)
+    assert not torch.isnan(dst).any()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all()
+
+    xg, bg = synth.gelu_input(333, 1536, torch.float16, seed=2)
+    buf, yg, pad = _guarded((333, 1536), torch.float16, float("nan"))
+    wgs.bias_gelu_tanh(xg.to(DEV), bg.to(DEV), out=yg)
+    assert not torch.isnan(yg).any()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all()
+
+
+# ----------------------------------------------------------- streams ----
+
+def test_runs_on_the_callers_stream():
+    """Work is ordered on the caller's current stream: a producer on a side
+    stream, the kernel on the same side stream, no device-wide sync."""
+    s = torch.cuda.Stream(device=DEV)
+    x = synth.ln_input(131040, 192, seed=1).to(DEV)
+    want = wgs.ln_fwd(x, EPS)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        z = torch.zeros_like(x)
+        z.copy_(x)                      # producer on s
+        y = wgs.ln_fwd(z, EPS)          # must run after the copy, on s
+        done = torch.cuda.Event()
+        done.record(s)
+    done.synchronize()
+    assert torch.equal(y.view(torch.int16), want.view(torch.int16))
+
+
+# ---------------------------------------------------- contract checks ----
+
+def test_python_contract_errors():
+    x = torch.zeros(4, 192, dtype=torch.float16, device=DEV)
+    with pytest.raises(RuntimeError, match="float16"):
+        wgs.ln_fwd(x.float())
+    with pytest.raises(RuntimeError, match="contiguous"):
+        wgs.ln_fwd(torch.zeros(192, 8, dtype=torch.float16, device=DEV).t())
+    with pytest.raises(RuntimeError, match="width"):
+        wgs.ln_fwd(torch.zeros(4, 100, dtype=torch.float16, device=DEV))
+    with pytest.raises(RuntimeError, match="bias"):
+        wgs.bias_gelu_tanh(torch.zeros(4, 8, device=DEV), torch.zeros(7, device=DEV))
+    with pytest.raises(RuntimeError, match="CUDA"):
+        wgs.bias_gelu_tanh(torch.zeros(4, 8, device=DEV), torch.zeros(8))
+    # empty inputs launch nothing and return empty outputs
+    assert wgs.ln_fwd(torch.zeros(0, 192, dtype=torch.float16, device=DEV)).shape == (0, 192)
+    assert wgs.bias_gelu_tanh(torch.zeros(0, 8, device=DEV), torch.zeros(8, device=DEV)).shape == (0, 8)
+    assert wgs.window_gather(x, torch.zeros(0, dtype=torch.int32, device=DEV)).shape == (0, 192)

@@ -1,1 +1,18 @@
-"""GB300-native block-glue kernels for shifted-window transformers."""
+"""GB300-native block-glue kernels for shifted-window transformers.
+
+No-affine LayerNorm, fused residual add + LayerNorm, the INT32-indexed
+shifted-window gather, the fused norm-then-gather and the bias + tanh-GELU
+epilogue, as hand-written sm_103a CUDA kernels behind a C ABI
+(include/wgs.h, libwgs.so).  The functions below are thin marshalling
+wrappers with the same names as the C entry points.
+"""
+from .api import (LN_WIDTHS, PAD_THEN_SHIFT, SHIFT_THEN_PAD, bias_gelu_tanh, build_window_index,
+                  check_error, ln_fwd, norm_gather, residual_add_ln_fwd, window_gather,
+                  window_index_count)
+from ._capi import WgsError
+
+__all__ = [
+    "ln_fwd", "residual_add_ln_fwd", "window_gather", "norm_gather", "bias_gelu_tanh",
+    "window_index_count", "build_window_index", "check_error", "WgsError", "LN_WIDTHS",
+    "SHIFT_THEN_PAD", "PAD_THEN_SHIFT",
+]

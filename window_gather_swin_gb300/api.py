@@ -1,0 +1,192 @@
+"""Python entry points, one per C-ABI function, with the same names.
+
+Each function checks what the C ABI cannot see (device, dtype, contiguity,
+shapes of torch tensors), allocates outputs the caller did not pass, and
+hands raw pointers plus the current CUDA stream of the tensors' device to
+libwgs.so.  No arithmetic of the op happens here, and there is no CPU path:
+CPU tensors are rejected.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _capi
+
+_DTYPE = {torch.float32: _capi.WGS_F32, torch.float16: _capi.WGS_F16}
+LN_WIDTHS = (192, 384)
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise RuntimeError(msg)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None) -> None:
+    _require(isinstance(t, torch.Tensor), f"{name} must be a torch.Tensor")
+    _require(t.is_cuda, f"{name} must be a CUDA tensor (got {t.device})")
+    if dtype is not None:
+        _require(t.dtype == dtype, f"{name} must be {dtype} (got {t.dtype})")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _same_device(*ts: torch.Tensor) -> None:
+    dev = ts[0].device
+    for t in ts[1:]:
+        _require(t.device == dev, f"all tensors must be on {dev} (got {t.device})")
+
+
+def _stream_ptr(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
+
+
+def _out(out: Optional[torch.Tensor], like_shape, dtype, device, name: str) -> torch.Tensor:
+    if out is None:
+        return torch.empty(like_shape, dtype=dtype, device=device)
+    _cuda(out, name, dtype)
+    _require(tuple(out.shape) == tuple(like_shape),
+             f"{name} must have shape {tuple(like_shape)} (got {tuple(out.shape)})")
+    return out
+
+
+def _rows_width(x: torch.Tensor, name: str):
+    _require(x.dim() >= 2, f"{name} must be [..., width]")
+    width = x.shape[-1]
+    return x.numel() // width if width else 0, width
+
+
+# ------------------------------------------------------------------ LN ----
+
+def ln_fwd(x: torch.Tensor, eps: float = 1e-5, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """No-affine LayerNorm over the last dim (192 or 384) of an fp16 tensor."""
+    _cuda(x, "x", torch.float16)
+    rows, width = _rows_width(x, "x")
+    _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
+    y = _out(out, x.shape, torch.float16, x.device, "out")
+    _same_device(x, y)
+    with torch.cuda.device(x.device):
+        _capi.check("ln_fwd", _capi.load().ln_fwd(_ptr(x), _ptr(y), rows, width, float(eps),
+                                                  _stream_ptr(x.device)))
+    return y
+
+
+def residual_add_ln_fwd(residual: torch.Tensor, branch: torch.Tensor, eps: float = 1e-5,
+                        residual_out: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None):
+    """Returns (residual_out, y): residual_out = fp16(residual + branch),
+    y = LN(residual_out)."""
+    _cuda(residual, "residual", torch.float16)
+    _cuda(branch, "branch", torch.float16)
+    _require(residual.shape == branch.shape, "residual and branch must have the same shape")
+    rows, width = _rows_width(residual, "residual")
+    _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
+    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
+    y = _out(out, residual.shape, torch.float16, residual.device, "out")
+    _same_device(residual, branch, r, y)
+    with torch.cuda.device(residual.device):
+        _capi.check("residual_add_ln_fwd", _capi.load().residual_add_ln_fwd(
+            _ptr(residual), _ptr(branch), _ptr(r), _ptr(y), rows, width, float(eps),
+            _stream_ptr(residual.device)))
+    return r, y
+
+
+# -------------------------------------------------------------- gather ----
+
+def _gather_args(src, idx, out, name):
+    _cuda(src, "src", torch.float16)
+    _cuda(idx, "idx", torch.int32)
+    _require(src.dim() == 2, "src must be [n_src, width]")
+    _require(idx.dim() == 1, "idx must be 1-D")
+    n_src, width = src.shape
+    dst = _out(out, (idx.numel(), width), torch.float16, src.device, "out")
+    _same_device(src, idx, dst)
+    return n_src, width, dst
+
+
+def window_gather(src: torch.Tensor, idx: torch.Tensor,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dst[d] = src[idx[d]] (idx >= 0) or a zero row (idx == -1)."""
+    n_src, width, dst = _gather_args(src, idx, out, "window_gather")
+    with torch.cuda.device(src.device):
+        _capi.check("window_gather", _capi.load().window_gather(
+            _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, _stream_ptr(src.device)))
+    return dst
+
+
+def norm_gather(src: torch.Tensor, idx: torch.Tensor, eps: float = 1e-5,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dst[d] = LN(src[idx[d]]) (idx >= 0) or a zero row (idx == -1)."""
+    n_src, width, dst = _gather_args(src, idx, out, "norm_gather")
+    _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
+    with torch.cuda.device(src.device):
+        _capi.check("norm_gather", _capi.load().norm_gather(
+            _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, float(eps),
+            _stream_ptr(src.device)))
+    return dst
+
+
+# ---------------------------------------------------------------- GELU ----
+
+def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """gelu_tanh(x + bias) over the last dim, fp32 or fp16."""
+    _cuda(x, "x")
+    _require(x.dtype in _DTYPE, f"x must be float32 or float16 (got {x.dtype})")
+    _cuda(bias, "bias", x.dtype)
+    _require(x.dim() >= 1, "x must have at least one dimension")
+    width = x.shape[-1]
+    _require(bias.dim() == 1 and bias.numel() == width,
+             f"bias must be 1-D with {width} elements (got shape {tuple(bias.shape)})")
+    rows = x.numel() // width if width else 0
+    y = _out(out, x.shape, x.dtype, x.device, "out")
+    _same_device(x, bias, y)
+    with torch.cuda.device(x.device):
+        _capi.check("bias_gelu_tanh", _capi.load().bias_gelu_tanh(
+            _ptr(x), _ptr(bias), _ptr(y), rows, width, _DTYPE[x.dtype], _stream_ptr(x.device)))
+    return y
+
+
+# ----------------------------------------------------------- index map ----
+
+SHIFT_THEN_PAD, PAD_THEN_SHIFT = 0, 1
+
+
+def _i3(v, name):
+    vals = [int(a) for a in v]
+    _require(len(vals) == 3, f"{name} must have 3 entries")
+    return (ctypes.c_int32 * 3)(*vals)
+
+
+def window_index_count(grid: Sequence[int], window: Sequence[int],
+                       padded: Optional[Sequence[int]] = None) -> int:
+    n = _capi.load().wgs_window_index_count(_i3(grid, "grid"), _i3(window, "window"),
+                                            _i3(padded, "padded") if padded is not None else None)
+    _require(n >= 0, "invalid grid / window / padded extents")
+    return int(n)
+
+
+def build_window_index(grid: Sequence[int], window: Sequence[int], shift: Sequence[int],
+                       padded: Optional[Sequence[int]] = None, flags: int = SHIFT_THEN_PAD,
+                       device=None) -> torch.Tensor:
+    """The INT32 destination -> source map (host-built); on `device` if given."""
+    n = window_index_count(grid, window, padded)
+    out = torch.empty(n, dtype=torch.int32)
+    _capi.check("wgs_build_window_index", _capi.load().wgs_build_window_index(
+        _i3(grid, "grid"), _i3(window, "window"), _i3(shift, "shift"),
+        _i3(padded, "padded") if padded is not None else None, int(flags),
+        ctypes.c_void_p(out.data_ptr()), n))
+    return out if device is None else out.to(device)
+
+
+def check_error(device=None) -> None:
+    """Raise if any gather on `device` met an index outside [-1, n_src)
+    since the last check.  Synchronises that device's current stream."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _capi.check("wgs_check_error", _capi.load().wgs_check_error(_stream_ptr(dev)))

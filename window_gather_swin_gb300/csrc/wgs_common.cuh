@@ -1,0 +1,90 @@
+// Shared host and device helpers of the sm_103a block-glue kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "wgs.h"
+
+namespace wgs {
+
+// ------------------------------------------------------------ host side --
+
+// Streaming multiprocessors of the current device (cached per device), or
+// a negative value on failure.  Also fails unless the device is compute
+// capability 10.3, the only target these kernels are built for.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+};
+wgs_status current_device(DeviceInfo *info);
+
+// Status of the launch just made on this thread.
+inline wgs_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? WGS_OK : WGS_ERR_LAUNCH;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// True when [a, a + na) and [b, b + nb) share a byte.
+inline bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + static_cast<uintptr_t>(nb) &&
+           y < x + static_cast<uintptr_t>(na);
+}
+
+// Same buffer exactly, or no shared byte at all.
+inline bool same_or_disjoint(const void *a, const void *b, int64_t n) {
+    return a == b || !overlap(a, n, b, n);
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------- device side --
+
+// 16-byte global load that skips L1 (each byte is read exactly once).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    return __ldcg(reinterpret_cast<const uint4 *>(p));
+}
+
+// 16-byte global store.
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+    *reinterpret_cast<uint4 *>(p) = v;
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t bits) {
+    __half2 h;
+    memcpy(&h, &bits, sizeof(h));
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t float2_to_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);  // round to nearest even
+    uint32_t bits;
+    memcpy(&bits, &h, sizeof(bits));
+    return bits;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4 &v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void set_word(uint4 &v, int j, uint32_t w) {
+    if (j == 0) v.x = w; else if (j == 1) v.y = w; else if (j == 2) v.z = w; else v.w = w;
+}
+
+// Sum over the LPR consecutive lanes that share a row (LPR a power of two,
+// groups aligned to LPR), by butterfly exchange; every lane of the group
+// ends with the total.  All 32 lanes must call it together.
+template <int LPR>
+__device__ __forceinline__ float group_sum(float s) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+}  // namespace wgs

@@ -1,0 +1,86 @@
+// Host-side construction of the shifted-window INT32 index map.
+//
+// Page "BW1000 gfx936 Pangu-Weather inference profiling", s5: the window
+// gather reads one precomputed INT32 per destination row; a value >= 0 names
+// the source token and -1 asks for a zero row, so shift, padding and the
+// window-major reordering all live in one array built once per window shape.
+// The construction (see wgs.h) walks the destination in order: window by
+// window, then cell by cell inside each window, writing each cell's source.
+#include "wgs.h"
+
+#include <cstdint>
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t wrap(int64_t a, int64_t m) {
+    int64_t r = a % m;
+    return r < 0 ? r + m : r;
+}
+
+bool padded_extents(const int32_t grid[3], const int32_t window[3], const int32_t *padded,
+                    int64_t ext[3]) {
+    for (int k = 0; k < 3; ++k) {
+        if (grid[k] < 1 || window[k] < 1) return false;
+        ext[k] = padded ? padded[k] : ceil_div(grid[k], window[k]) * window[k];
+        if (ext[k] < grid[k]) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" int64_t wgs_window_index_count(const int32_t grid[3], const int32_t window[3],
+                                          const int32_t *padded) {
+    if (!grid || !window) return -1;
+    int64_t ext[3];
+    if (!padded_extents(grid, window, padded, ext)) return -1;
+    return ext[0] * ext[1] * ext[2];
+}
+
+extern "C" wgs_status wgs_build_window_index(const int32_t grid[3], const int32_t window[3],
+                                             const int32_t shift[3], const int32_t *padded,
+                                             int32_t flags, int32_t *out_host, int64_t out_len) {
+    if (!grid || !window || !shift || !out_host) return WGS_ERR_NULL;
+    if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
+    int64_t ext[3];
+    if (!padded_extents(grid, window, padded, ext)) return WGS_ERR_SHAPE;
+    const int64_t G[3] = {grid[0], grid[1], grid[2]};
+    if (G[0] * G[1] * G[2] > INT32_MAX) return WGS_ERR_SHAPE;
+    if (out_len < ext[0] * ext[1] * ext[2]) return WGS_ERR_SHAPE;
+
+    // The roll is taken modulo the grid (shift then pad) or the padded grid
+    // (pad then shift).
+    const bool roll_padded = flags == WGS_PAD_THEN_SHIFT;
+    int64_t period[3], s[3];
+    for (int k = 0; k < 3; ++k) {
+        period[k] = roll_padded ? ext[k] : G[k];
+        s[k] = wrap(shift[k], period[k]);
+    }
+
+    int64_t d = 0;
+    for (int64_t z0 = 0; z0 < ext[0]; z0 += window[0])
+        for (int64_t h0 = 0; h0 < ext[1]; h0 += window[1])
+            for (int64_t w0 = 0; w0 < ext[2]; w0 += window[2]) {
+                const int64_t z1 = z0 + window[0] < ext[0] ? z0 + window[0] : ext[0];
+                const int64_t h1 = h0 + window[1] < ext[1] ? h0 + window[1] : ext[1];
+                const int64_t w1 = w0 + window[2] < ext[2] ? w0 + window[2] : ext[2];
+                for (int64_t z = z0; z < z1; ++z)
+                    for (int64_t h = h0; h < h1; ++h)
+                        for (int64_t w = w0; w < w1; ++w) {
+                            int32_t v = -1;
+                            const bool inside = z < G[0] && h < G[1] && w < G[2];
+                            if (roll_padded || inside) {
+                                int64_t zs = z + s[0], hs = h + s[1], ws = w + s[2];
+                                if (zs >= period[0]) zs -= period[0];
+                                if (hs >= period[1]) hs -= period[1];
+                                if (ws >= period[2]) ws -= period[2];
+                                if (zs < G[0] && hs < G[1] && ws < G[2])
+                                    v = static_cast<int32_t>((zs * G[1] + hs) * G[2] + ws);
+                            }
+                            out_host[d++] = v;
+                        }
+            }
+    return WGS_OK;
+}

@@ -1,0 +1,326 @@
+// Row kernels of the block glue: no-affine LayerNorm, fused residual add +
+// LayerNorm, shifted-window gather and fused norm-then-gather (sm_103a).
+//
+// Page "BW1000 gfx936 Pangu-Weather inference profiling":
+//   s3  fixed-width (192 / 384) LayerNorm, FP16 in and out, FP32 statistics
+//   s4  residual add + norm that keeps the FP16 rounding point
+//   s5  INT32-indexed window gather (-1 = zero row) and the fused
+//       norm-gather that never writes the normalised tensor
+//
+// Design (GB300): all four are HBM-bound row streams, so there are no tensor
+// cores here.  A row of W fp16 values is W/8 16-byte chunks; LPR lanes share
+// a row (8 lanes at W = 192, 16 at W = 384), each holding CPL = 3 chunks in
+// registers, so one warp-wide load instruction moves whole 128-byte lines.
+// The row never leaves registers between load, FP32 butterfly reductions and
+// store.  Each warp works on U row groups at once so that every lane has
+// U * CPL independent 16-byte loads in flight before its first reduction.
+#include "wgs_common.cuh"
+
+#ifndef WGS_ROW_WARPS
+#define WGS_ROW_WARPS 4      // warps per CTA
+#endif
+#ifndef WGS_ROW_U
+#define WGS_ROW_U 2          // row groups per warp per iteration
+#endif
+#ifndef WGS_ROW_CTAS_PER_SM
+#define WGS_ROW_CTAS_PER_SM 64  // grid cap, in CTAs per SM (grid-stride beyond it)
+#endif
+
+namespace wgs {
+
+// Set (never cleared by a kernel) when a gather meets an index outside
+// [-1, n_src); read and cleared by wgs_check_error().
+__device__ unsigned int g_index_error;
+
+enum class RowOp : int { kLN, kAddLN, kGather, kNormGather };
+
+struct RowArgs {
+    const __half *in0;    // x (LN), residual (add + LN), src (gathers)
+    const __half *in1;    // branch (add + LN)
+    __half *out0;         // y (LN), residual_out (add + LN), dst (gathers)
+    __half *out1;         // y (add + LN)
+    const int32_t *idx;   // gathers
+    int64_t rows;         // rows (LN, add + LN) or n_idx (gathers)
+    int64_t n_src;        // gathers
+    float eps;
+};
+
+template <int WIDTH> struct RowTiling;
+template <> struct RowTiling<192> { static constexpr int kLPR = 8; };
+template <> struct RowTiling<384> { static constexpr int kLPR = 16; };
+
+// No-affine LayerNorm of U rows per lane group, each row held as CPL chunks
+// per lane over LPR lanes: mean and biased variance in FP32 (two passes over
+// the registers), y = fp16((x - mean) * (1 / sqrt(var + eps))).  Every LN
+// kernel calls this one function, so equal inputs give equal bits.
+template <int WIDTH, int LPR, int CPL, int U>
+__device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
+    float mean[U], rstd[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = half2_to_float2(word(v[u][k], j));
+                s += f.x;
+                s += f.y;
+            }
+        mean[u] = s;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) mean[u] = group_sum<LPR>(mean[u]) / static_cast<float>(WIDTH);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = half2_to_float2(word(v[u][k], j));
+                const float dx = f.x - mean[u], dy = f.y - mean[u];
+                q = fmaf(dx, dx, q);
+                q = fmaf(dy, dy, q);
+            }
+        rstd[u] = q;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float var = group_sum<LPR>(rstd[u]) / static_cast<float>(WIDTH);
+        rstd[u] = 1.0f / sqrtf(var + eps);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int k = 0; k < CPL; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = half2_to_float2(word(v[u][k], j));
+                set_word(v[u][k], j,
+                         float2_to_half2((f.x - mean[u]) * rstd[u], (f.y - mean[u]) * rstd[u]));
+            }
+}
+
+template <RowOp OP, int WIDTH, int U, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
+    constexpr int LPR = RowTiling<WIDTH>::kLPR;
+    constexpr int CPL = WIDTH / 8 / LPR;
+    constexpr int RPW = 32 / LPR;                 // rows per warp per group
+    constexpr int ROWS_CTA = WARPS * RPW * U;     // rows per CTA per iteration
+    constexpr bool kGatherOp = OP == RowOp::kGather || OP == RowOp::kNormGather;
+    constexpr bool kNorm = OP != RowOp::kGather;
+    static_assert(LPR * CPL * 8 == WIDTH, "row tiling must cover the row");
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int grp = lane / LPR;
+    const int sub = lane % LPR;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * ROWS_CTA;
+
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * ROWS_CTA; base < a.rows;
+         base += stride) {
+        int64_t row[U], src[U];
+        bool live[U], valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            row[u] = base + static_cast<int64_t>(warp * U + u) * RPW + grp;
+            live[u] = row[u] < a.rows;
+            src[u] = row[u];
+            valid[u] = live[u];
+        }
+        if constexpr (kGatherOp) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t s = live[u] ? __ldg(a.idx + row[u]) : -1;
+                valid[u] = s >= 0 && s < a.n_src;
+                if (live[u] && !valid[u] && s != -1 && sub == 0) atomicOr(&g_index_error, 1u);
+                src[u] = valid[u] ? s : 0;
+            }
+        }
+
+        uint4 v[U][CPL];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < CPL; ++k)
+                v[u][k] = valid[u] ? ld_stream(a.in0 + src[u] * WIDTH + (sub + k * LPR) * 8) : zero;
+
+        if constexpr (OP == RowOp::kAddLN) {
+            uint4 b[U][CPL];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+                    b[u][k] = valid[u] ? ld_stream(a.in1 + row[u] * WIDTH + (sub + k * LPR) * 8)
+                                       : zero;
+            // residual_out = fp16(fp32 residual + fp32 branch)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 x = half2_to_float2(word(v[u][k], j));
+                        const float2 y = half2_to_float2(word(b[u][k], j));
+                        set_word(v[u][k], j, float2_to_half2(x.x + y.x, x.y + y.y));
+                    }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (live[u])
+#pragma unroll
+                    for (int k = 0; k < CPL; ++k)
+                        st_stream(a.out0 + row[u] * WIDTH + (sub + k * LPR) * 8, v[u][k]);
+        }
+
+        if constexpr (kNorm) ln_normalize<WIDTH, LPR, CPL, U>(v, a.eps);
+
+        __half *out = OP == RowOp::kAddLN ? a.out1 : a.out0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (live[u])
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+                    st_stream(out + row[u] * WIDTH + (sub + k * LPR) * 8, valid[u] ? v[u][k] : zero);
+    }
+}
+
+// Gather for any width that is a whole number of 16-byte chunks: one warp
+// per destination row, lanes striding over the row's chunks.
+__global__ void __launch_bounds__(256) gather_any_width_kernel(const uint4 *src, const int32_t *idx,
+                                                                uint4 *dst, int64_t n_src,
+                                                                int64_t n_idx, int32_t chunks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t d = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         d < n_idx; d += warps) {
+        const int32_t s = __ldg(idx + d);
+        const bool valid = s >= 0 && s < n_src;
+        if (!valid && s != -1 && lane == 0) atomicOr(&g_index_error, 1u);
+        for (int c = lane; c < chunks; c += 32)
+            dst[d * chunks + c] = valid ? ld_stream(src + static_cast<int64_t>(s) * chunks + c)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <RowOp OP, int WIDTH>
+wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
+    constexpr int U = WGS_ROW_U, WARPS = WGS_ROW_WARPS;
+    constexpr int ROWS_CTA = WARPS * (32 / RowTiling<WIDTH>::kLPR) * U;
+    DeviceInfo dev;
+    const wgs_status st = current_device(&dev);
+    if (st != WGS_OK) return st;
+    const int64_t iters = ceil_div(a.rows, ROWS_CTA);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
+    const unsigned grid = static_cast<unsigned>(iters < cap ? iters : cap);
+    row_kernel<OP, WIDTH, U, WARPS><<<grid, WARPS * 32, 0, stream>>>(a);
+    return launch_status();
+}
+
+template <RowOp OP>
+wgs_status dispatch_width(const RowArgs &a, int32_t width, cudaStream_t stream) {
+    return width == 192 ? launch_rows<OP, 192>(a, stream) : launch_rows<OP, 384>(a, stream);
+}
+
+bool ln_width(int32_t width) { return width == 192 || width == 384; }
+
+// rows * width fp16 values must be addressable in bytes.
+bool fits(int64_t rows, int32_t width) { return rows <= INT64_MAX / 2 / width; }
+
+}  // namespace wgs
+
+using namespace wgs;
+
+extern "C" wgs_status ln_fwd(const void *x, void *y, int64_t rows, int32_t width, float eps,
+                             cudaStream_t stream) {
+    if (!ln_width(width)) return WGS_ERR_WIDTH;
+    if (rows < 0 || !fits(rows, width)) return WGS_ERR_SHAPE;
+    if (rows == 0) return WGS_OK;
+    if (!x || !y) return WGS_ERR_NULL;
+    if (!aligned16(x) || !aligned16(y)) return WGS_ERR_ALIGN;
+    const int64_t bytes = rows * width * 2;
+    if (!same_or_disjoint(x, y, bytes)) return WGS_ERR_ALIAS;
+    RowArgs a{static_cast<const __half *>(x), nullptr, static_cast<__half *>(y), nullptr,
+              nullptr, rows, 0, eps};
+    return dispatch_width<RowOp::kLN>(a, width, stream);
+}
+
+extern "C" wgs_status residual_add_ln_fwd(const void *residual, const void *branch,
+                                          void *residual_out, void *y, int64_t rows,
+                                          int32_t width, float eps, cudaStream_t stream) {
+    if (!ln_width(width)) return WGS_ERR_WIDTH;
+    if (rows < 0 || !fits(rows, width)) return WGS_ERR_SHAPE;
+    if (rows == 0) return WGS_OK;
+    if (!residual || !branch || !residual_out || !y) return WGS_ERR_NULL;
+    if (!aligned16(residual) || !aligned16(branch) || !aligned16(residual_out) || !aligned16(y))
+        return WGS_ERR_ALIGN;
+    const int64_t bytes = rows * width * 2;
+    if (overlap(residual_out, bytes, y, bytes)) return WGS_ERR_ALIAS;
+    if (!same_or_disjoint(residual_out, residual, bytes) ||
+        !same_or_disjoint(residual_out, branch, bytes) || !same_or_disjoint(y, residual, bytes) ||
+        !same_or_disjoint(y, branch, bytes))
+        return WGS_ERR_ALIAS;
+    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(branch),
+              static_cast<__half *>(residual_out), static_cast<__half *>(y), nullptr, rows, 0, eps};
+    return dispatch_width<RowOp::kAddLN>(a, width, stream);
+}
+
+namespace {
+
+wgs_status check_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                        int64_t n_idx, int32_t width) {
+    if (n_src < 0 || n_idx < 0 || !fits(n_src, width) || !fits(n_idx, width)) return WGS_ERR_SHAPE;
+    if (n_idx == 0) return WGS_OK;
+    if (!idx || !dst || (n_src > 0 && !src)) return WGS_ERR_NULL;
+    if (!aligned16(dst) || (src && !aligned16(src)) || !aligned4(idx)) return WGS_ERR_ALIGN;
+    const int64_t dst_bytes = n_idx * width * 2;
+    if (overlap(src, n_src * width * 2, dst, dst_bytes) || overlap(idx, n_idx * 4, dst, dst_bytes))
+        return WGS_ERR_ALIAS;
+    return WGS_OK;
+}
+
+}  // namespace
+
+extern "C" wgs_status window_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                                    int64_t n_idx, int32_t width, cudaStream_t stream) {
+    if (width <= 0 || width % 8 != 0) return WGS_ERR_WIDTH;
+    wgs_status st = check_gather(src, idx, dst, n_src, n_idx, width);
+    if (st != WGS_OK || n_idx == 0) return st;
+    RowArgs a{static_cast<const __half *>(src), nullptr, static_cast<__half *>(dst), nullptr, idx,
+              n_idx, n_src, 0.f};
+    if (ln_width(width)) return dispatch_width<RowOp::kGather>(a, width, stream);
+
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != WGS_OK) return st;
+    const int64_t warps_needed = n_idx;
+    const int64_t blocks = ceil_div(warps_needed, 8);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    gather_any_width_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
+        static_cast<const uint4 *>(src), idx, static_cast<uint4 *>(dst), n_src, n_idx, width / 8);
+    return launch_status();
+}
+
+extern "C" wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                                  int64_t n_idx, int32_t width, float eps, cudaStream_t stream) {
+    if (!ln_width(width)) return WGS_ERR_WIDTH;
+    const wgs_status st = check_gather(src, idx, dst, n_src, n_idx, width);
+    if (st != WGS_OK || n_idx == 0) return st;
+    RowArgs a{static_cast<const __half *>(src), nullptr, static_cast<__half *>(dst), nullptr, idx,
+              n_idx, n_src, eps};
+    return dispatch_width<RowOp::kNormGather>(a, width, stream);
+}
+
+extern "C" wgs_status wgs_check_error(cudaStream_t stream) {
+    unsigned int seen = 0;
+    const unsigned int cleared = 0;
+    if (cudaMemcpyFromSymbolAsync(&seen, g_index_error, sizeof(seen), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess)
+        return WGS_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_index_error, &cleared, sizeof(cleared), 0,
+                                cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return WGS_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return WGS_ERR_CUDA;
+    return seen ? WGS_ERR_INDEX : WGS_OK;
+}
