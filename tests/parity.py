@@ -1,26 +1,28 @@
 """Comparison rules between the CUDA path and the oracle.
 
 * Bitwise outputs (residual_out, gathered rows, pad rows): identical bits.
-* LayerNorm outputs (fp16): max |gpu - oracle| <= 2e-3 (about one fp16 ulp
-  near 1).  Above that, and independently of it, every element that differs
-  from the oracle's fp16 value must be its immediate fp16 neighbour AND the
-  oracle's unrounded value must sit within TIE_REL * |y| + tie_abs of the
-  midpoint between the two: the kernel computes in FP32, so it can only land
-  on the other side of a rounding boundary when the exact value is that
-  close to it.  For LN, tie_abs = LN_TIE_ABS covers the absolute error of
-  x - mean in FP32 (the mean of 192 or 384 values of magnitude up to ~8 is
-  good to about 3e-7); the rule is stricter than the 2e-3 bound wherever
-  |y| < 0.5.
-* fp32 GELU: |gpu - y64| <= 1e-5 |y64| + FLT_MIN (the floor only matters for
+* fp16 outputs computed in FP32 (LayerNorm, fp16 GELU): every element obeys
+      |gpu - y| <= ulp16(gpu) / 2 + TIE_REL * |y| + tie_abs,
+  where y is the oracle's unrounded double value: the kernel's FP32 result
+  is within TIE_REL relative plus tie_abs absolute of y, and rounding it to
+  fp16 adds at most half a spacing.  For LayerNorm the absolute term
+  LN_TIE_ABS covers the FP32 error of d = x - mean, which dominates near
+  y = 0 where fp16 spacings are tiny: with the shifted-data two-pass (sums
+  of x - x[0]), recursive summation over at most ~27 levels bounds the
+  error of the mean by ~27 u * 1.5 sigma (u = 2^-24), i.e. about 2.4e-6
+  after scaling by 1/sigma; LN_TIE_ABS = 4e-6 leaves margin.
+* LayerNorm additionally meets the 2e-3 max-abs bar, except for elements
+  one fp16 spacing away from the oracle's fp16 value whose unrounded value
+  lies within TIE_REL * |y| + tie_abs of the midpoint (legitimate rounding
+  flips at |y| >= 4, where one spacing is 3.9e-3).
+* fp32 GELU: |gpu - y| <= 1e-5 |y| + FLT_MIN (the floor only matters for
   results that underflow single precision).
-* fp16 GELU: within one fp16 ulp of fp16(y64), and every differing element
-  is a near-tie in the same sense as LN.
 """
 import numpy as np
 
 LN_ABS_TOL = 2e-3
 TIE_REL = 1e-5
-LN_TIE_ABS = 2e-6
+LN_TIE_ABS = 4e-6
 GELU_TIE_ABS = 1e-12
 GELU_F32_REL = 1e-5
 FLT_MIN = float(np.finfo(np.float32).tiny)
@@ -52,27 +54,44 @@ def _near_tie(g: np.ndarray, o16: np.ndarray, y64: np.ndarray, tie_abs: float) -
     return np.abs(y64 - mid) <= TIE_REL * np.abs(y64) + tie_abs
 
 
+def fp16_spacing(v: np.ndarray) -> np.ndarray:
+    """Distance from |v| to the next larger fp16 value (2^-24 below 2^-14)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10.0)
+
+
 def check_fp16_near(gpu: np.ndarray, o16: np.ndarray, y64: np.ndarray, what: str,
                     abs_tol=None, tie_abs: float = GELU_TIE_ABS) -> dict:
-    """fp16 outputs against the oracle's rounded and unrounded values."""
+    """fp16 outputs against the oracle's rounded (o16) and unrounded (y64) values."""
     assert gpu.shape == o16.shape == y64.shape, what
-    nan_g, nan_o = np.isnan(gpu.astype(np.float32)), np.isnan(o16.astype(np.float32))
-    assert np.array_equal(nan_g, nan_o), f"{what}: NaN positions differ"
-    ok = ~nan_g
-    g, o, y = gpu[ok], o16[ok], y64[ok]
+    gf = gpu.astype(np.float64)
+    of = o16.astype(np.float64)
+    fin = np.isfinite(of)
+    assert np.array_equal(np.isnan(gf), np.isnan(of)), f"{what}: NaN positions differ"
+    inf = np.isinf(of)
+    assert np.array_equal(gf[inf], of[inf]), f"{what}: infinities differ"
+    g, o, y = gpu[fin], o16[fin], y64[fin]
+    gd = g.astype(np.float64)
     dist = ulp_distance(g, o)
-    diff = np.abs(g.astype(np.float64) - o.astype(np.float64))
-    mism = dist > 0
-    stats = {"n": int(g.size), "mismatches": int(mism.sum()), "max_ulp": int(dist.max(initial=0)),
-             "max_abs": float(diff.max(initial=0.0))}
-    assert stats["max_ulp"] <= 1, f"{what}: {stats}"
-    if mism.any():
-        tie = _near_tie(g[mism], o[mism], y[mism], tie_abs)
-        assert tie.all(), (f"{what}: {int((~tie).sum())} one-ulp differences are not near a "
-                           f"rounding midpoint; {stats}")
-    if abs_tol is not None and stats["max_abs"] > abs_tol:
-        # only near-tie one-ulp flips (checked above) may exceed the bound
-        stats["above_abs_tol"] = int((diff > abs_tol).sum())
+    diff = np.abs(gd - o.astype(np.float64))
+    err = np.abs(gd - y)
+    bound = 0.5 * fp16_spacing(gd) + TIE_REL * np.abs(y) + tie_abs
+    viol = err > bound
+    stats = {"n": int(g.size), "mismatches": int((dist > 0).sum()),
+             "max_ulp": int(dist.max(initial=0)), "max_abs": float(diff.max(initial=0.0)),
+             "max_err_over_bound": float((err / bound).max(initial=0.0))}
+    if viol.any():
+        k = np.argmax(err - bound)
+        raise AssertionError(f"{what}: {int(viol.sum())} elements outside the FP32 error bound, "
+                             f"worst gpu={gd[k]!r} oracle={y[k]!r}; {stats}")
+    if abs_tol is not None:
+        above = diff > abs_tol
+        if above.any():
+            ok = (dist[above] == 1) & _near_tie(g[above], o[above], y[above], tie_abs)
+            assert ok.all(), (f"{what}: {int((~ok).sum())} elements exceed {abs_tol} without "
+                              f"being a one-spacing rounding flip at a midpoint; {stats}")
+            stats["above_abs_tol_tie_flips"] = int(above.sum())
     return stats
 
 

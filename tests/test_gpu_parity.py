@@ -69,6 +69,20 @@ def test_ln_ragged_rows(rows, width):
     check_ln(np_(y), oracle.ln(x.numpy(), EPS), oracle.ln_f64(x.numpy(), EPS), f"ln {rows}x{width}")
 
 
+@pytest.mark.parametrize("width", [192, 384])
+@pytest.mark.parametrize("offset", [0.0, 2.0, -7.5])
+def test_ln_rows_with_variance_near_eps(width, offset):
+    """Spread ~0.003 (variance ~ eps) around an offset: a misplaced eps or a
+    centring error shows at full scale here."""
+    z = synth.gather_source(999, width, seed=int(offset * 10) + width).float()
+    x = (offset + 0.003 * z).to(torch.float16)
+    for fn in (lambda t: wgs.ln_fwd(t, EPS),
+               lambda t: wgs.residual_add_ln_fwd(t, torch.zeros_like(t), EPS)[1]):
+        y = fn(x.to(DEV))
+        check_ln(np_(y), oracle.ln(x.numpy(), EPS), oracle.ln_f64(x.numpy(), EPS),
+                 f"ln small var offset {offset}")
+
+
 @pytest.mark.parametrize("stage", [synth.STAGE_192, synth.STAGE_384], ids=lambda s: s.name)
 def test_ln_full_size(stage):
     x = synth.ln_input(stage.tokens, stage.width, seed=1)

@@ -340,3 +340,39 @@ def test_gelu_f16_rounding_point():
     ref = _torch_gelu64(t16.astype(np.float64))
     assert np.max(np.abs(y64 - ref) / np.maximum(np.abs(ref), 1e-300)) < 1e-13
     assert np.array_equal(y.view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+# ------------------------------------------------ the comparison rules ----
+
+def _ln_fp32_shifted(x16, eps=EPS, unbiased=False, drop_eps=False):
+    """An FP32 LayerNorm by the shifted-data two-pass method, in numpy."""
+    x = x16.astype(np.float32)
+    k = x[:, :1]
+    xs = x - k
+    m = xs.mean(axis=1, keepdims=True, dtype=np.float32)
+    d = xs - m
+    n = x.shape[1] - (1 if unbiased else 0)
+    var = (d * d).sum(axis=1, keepdims=True, dtype=np.float32) / np.float32(n)
+    rstd = np.float32(1) / np.sqrt(var + (np.float32(0) if drop_eps else np.float32(eps)))
+    return (d * rstd).astype(np.float16)
+
+
+def test_parity_rules_accept_fp32_rounding_and_reject_real_errors():
+    """The fp16 comparison accepts what an FP32 evaluation produces and
+    rejects a missing eps, an unbiased variance or a one-ulp bias."""
+    from parity import check_fp16_near, check_ln
+    x = synth.ln_input(256, 192, seed=12).numpy()
+    y64, o16 = oracle.ln_f64(x, EPS), oracle.ln(x, EPS)
+    check_ln(_ln_fp32_shifted(x), o16, y64, "fp32 evaluation")
+    with pytest.raises(AssertionError):
+        check_ln(_ln_fp32_shifted(x, unbiased=True), o16, y64, "unbiased variance")
+    bumped = (o16.view(np.uint16) + (o16.view(np.uint16) % 7 == 0)).view(np.float16)
+    with pytest.raises(AssertionError):
+        check_fp16_near(bumped, o16, y64, "one ulp off")
+    # rows with an offset and a variance close to eps expose an eps mistake
+    xs = (np.float32(2.0) + synth.gather_source(256, 192, seed=2).numpy().astype(np.float32)
+          * np.float32(0.003)).astype(np.float16)
+    ys64, ys16 = oracle.ln_f64(xs, EPS), oracle.ln(xs, EPS)
+    check_ln(_ln_fp32_shifted(xs), ys16, ys64, "small variance")
+    with pytest.raises(AssertionError):
+        check_ln(_ln_fp32_shifted(xs, drop_eps=True), ys16, ys64, "eps dropped")

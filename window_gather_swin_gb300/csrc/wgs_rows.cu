@@ -12,7 +12,8 @@
 // a row (8 lanes at W = 192, 16 at W = 384), each holding CPL = 3 chunks in
 // registers, so one warp-wide load instruction moves whole 128-byte lines.
 // The row never leaves registers between load, FP32 butterfly reductions and
-// store.  Each warp works on U row groups at once so that every lane has
+// store; the statistics use the shifted-data two-pass method (see
+// ln_normalize).  Each warp works on U row groups at once so that every lane has
 // U * CPL independent 16-byte loads in flight before its first reduction.
 #include "wgs_common.cuh"
 
@@ -50,12 +51,22 @@ template <> struct RowTiling<192> { static constexpr int kLPR = 8; };
 template <> struct RowTiling<384> { static constexpr int kLPR = 16; };
 
 // No-affine LayerNorm of U rows per lane group, each row held as CPL chunks
-// per lane over LPR lanes: mean and biased variance in FP32 (two passes over
-// the registers), y = fp16((x - mean) * (1 / sqrt(var + eps))).  Every LN
-// kernel calls this one function, so equal inputs give equal bits.
+// per lane over LPR lanes.  FP32 statistics by the shifted-data two-pass
+// method (Chan, Golub & LeVeque, "Algorithms for computing the sample
+// variance", 1983): with K the row's first element,
+//     m = sum(x - K) / W,  d = (x - K) - m,  var = sum(d^2) / W,
+//     y = fp16(d * (1 / sqrt(var + eps))).
+// Mathematically d = x - mean; numerically the shift keeps the summed terms
+// at the scale of the row's spread instead of its offset, so the rounding
+// error of d no longer grows with |mean|.  Every LN kernel calls this one
+// function, so equal inputs give equal bits.
 template <int WIDTH, int LPR, int CPL, int U>
 __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
-    float mean[U], rstd[U];
+    const int lead = (threadIdx.x & 31) & ~(LPR - 1);  // lane holding the row's first chunk
+    float shift[U], mean[U], rstd[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        shift[u] = __shfl_sync(0xffffffffu, half2_to_float2(v[u][0].x).x, lead);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         float s = 0.f;
@@ -64,8 +75,8 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 f = half2_to_float2(word(v[u][k], j));
-                s += f.x;
-                s += f.y;
+                s += f.x - shift[u];
+                s += f.y - shift[u];
             }
         mean[u] = s;
     }
@@ -79,7 +90,7 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 f = half2_to_float2(word(v[u][k], j));
-                const float dx = f.x - mean[u], dy = f.y - mean[u];
+                const float dx = (f.x - shift[u]) - mean[u], dy = (f.y - shift[u]) - mean[u];
                 q = fmaf(dx, dx, q);
                 q = fmaf(dy, dy, q);
             }
@@ -98,7 +109,8 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
             for (int j = 0; j < 4; ++j) {
                 const float2 f = half2_to_float2(word(v[u][k], j));
                 set_word(v[u][k], j,
-                         float2_to_half2((f.x - mean[u]) * rstd[u], (f.y - mean[u]) * rstd[u]));
+                         float2_to_half2(((f.x - shift[u]) - mean[u]) * rstd[u],
+                                         ((f.y - shift[u]) - mean[u]) * rstd[u]));
             }
 }
 
