@@ -304,11 +304,22 @@ int64_t orc_norm_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst,
 /* Bias + tanh-approximate GELU  [P3 s3]                               */
 /* ------------------------------------------------------------------ */
 
-/* gelu(t) = 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3))) */
+/* gelu(t) = 0.5 t (1 + tanh(u)),  u = sqrt(2/pi) (t + 0.044715 t^3).
+ * For u < 0 the sum 1 + tanh(u) cancels (in double it is exactly 0 once
+ * u < -18.7, i.e. t < -5.6 gives a wrong result long before that), so there
+ * it is evaluated through the exact identity 1 + tanh(u) = 2 e^{2u} / (1 + e^{2u}). */
 static double gelu_tanh(double t)
 {
     const double k = sqrt(2.0 / acos(-1.0));
-    return 0.5 * t * (1.0 + tanh(k * (t + 0.044715 * t * t * t)));
+    const double u = k * (t + 0.044715 * t * t * t);
+    double one_plus_tanh;
+    if (u >= 0.0) {
+        one_plus_tanh = 1.0 + tanh(u);
+    } else {
+        const double e = exp(2.0 * u);
+        one_plus_tanh = 2.0 * e / (1.0 + e);
+    }
+    return 0.5 * t * one_plus_tanh;
 }
 
 /* fp32: t = fp32(x + bias[col]) (the sum of two floats rounded once to
