@@ -318,7 +318,7 @@ def run_ours(args, rank, world, local):
 
     def flush():
         flush_w.zero_()
-        torch.sum(flush_r, out=sink)
+        torch.sum(flush_r, dim=0, out=sink)
 
     stream = torch.cuda.current_stream(dev)
     # warm-up (untimed)
