@@ -4,11 +4,21 @@
 // must equal gelu(input + bias, approximate="tanh"), i.e.
 //     t = x + bias[col],  y = 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3))).
 //
-// Evaluation: 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)) holds exactly, so
-//     y = t / (1 + exp(z)),   z = -2u = t (k1 + k3 t^2),
-//     k1 = -2 sqrt(2/pi),  k3 = -2 sqrt(2/pi) 0.044715.
-// This avoids the cancellation of 1 + tanh(u) for negative t (where it
-// tends to 0) and costs one exponential and one fast division per element.
+// Evaluation.  0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)) holds exactly, and
+// exp(v) = 2^(v log2 e), so
+//     y = t / (1 + 2^w),   w = -2u log2 e = t (c1 + c3 t^2),
+//     c1 = -2 sqrt(2/pi) log2 e,  c3 = -2 sqrt(2/pi) 0.044715 log2 e.
+// The power of two and the reciprocal are the PTX ex2.approx and
+// rcp.approx instructions (one MUFU operation each, relative error near
+// 2^-22), so an element costs about ten instructions: fp16 data carries
+// eight elements per 16 bytes, and a full-precision exp / divide would make
+// the kernel issue-bound instead of HBM-bound.  The form has no
+// cancellation for negative t, where 1 + tanh(u) tends to 0.
+//
+// Below t = -4, w exceeds 15 and grows like |t|^3, so an FP32 w carries an
+// absolute error of |w| times a few ulp, which 2^w turns into a relative
+// error of the result approaching 1e-5.  Those inputs (about 3e-5 of an
+// N(0,1) tensor) are recomputed from the same formula in FP64.
 //
 // The op streams 2 x rows x width elements through HBM; the vector path
 // moves 16-byte chunks and keeps U independent chunks in flight per thread.
@@ -27,42 +37,84 @@
 
 namespace wgs {
 
-// Below t = -4 the exponent z exceeds ~11 and grows like |t|^3; an FP32 z
-// then carries an absolute error of |z| * (a few ulp), which the exponential
-// turns into a relative error of the result approaching 1e-5.  Those inputs
-// (about 3e-5 of an N(0,1) tensor) take the same formula in FP64 instead.
+constexpr double kSqrt2OverPi = 0.7978845608028654;
+constexpr double kLog2e = 1.4426950408889634;
+constexpr float kFarLeft = -4.0f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Valid for t >= kFarLeft (and for +inf and NaN).
+__device__ __forceinline__ float gelu_tanh_fast(float t) {
+    constexpr float c1 = static_cast<float>(-2.0 * kSqrt2OverPi * kLog2e);
+    constexpr float c3 = static_cast<float>(-2.0 * kSqrt2OverPi * 0.044715 * kLog2e);
+    const float w = t * fmaf(c3, t * t, c1);
+    return t * rcp_approx(1.0f + ex2_approx(w));
+}
+
+// Any t, in FP64 (taken only for t < kFarLeft).
 __device__ __noinline__ float gelu_tanh_far_left(float t) {
-    constexpr double kSqrt2OverPi = 0.7978845608028654;
     const double td = t;
     const double z = td * (-2.0 * kSqrt2OverPi) * (1.0 + 0.044715 * td * td);
     return static_cast<float>(td / (1.0 + exp(z)));
 }
 
 __device__ __forceinline__ float gelu_tanh(float t) {
-    constexpr double kSqrt2OverPi = 0.7978845608028654;
-    constexpr float k1 = static_cast<float>(-2.0 * kSqrt2OverPi);
-    constexpr float k3 = static_cast<float>(-2.0 * kSqrt2OverPi * 0.044715);
-    if (t < -4.0f) return gelu_tanh_far_left(t);
-    const float z = t * fmaf(k3, t * t, k1);
-    return __fdividef(t, 1.0f + expf(z));
+    return t < kFarLeft ? gelu_tanh_far_left(t) : gelu_tanh_fast(t);
 }
 
 // One 16-byte chunk: 4 fp32 or 8 fp16 elements and the matching bias chunk.
+// The fast formula runs on every element; the rare far-left elements are
+// redone afterwards behind one branch per chunk.
 template <bool kHalf>
 __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
-    uint4 out;
+    constexpr int kN = kHalf ? 8 : 4;
+    float t[kN], y[kN];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if constexpr (kHalf) {
-            const float2 x = half2_to_float2(word(xv, j));
-            const float2 b = half2_to_float2(word(bv, j));
-            // t is rounded to fp16 first, as an unfused fp16 add would leave it
-            const float2 t = half2_to_float2(float2_to_half2(x.x + b.x, x.y + b.y));
-            set_word(out, j, float2_to_half2(gelu_tanh(t.x), gelu_tanh(t.y)));
+            // t = fp16(x + b): one correctly rounded fp16 add, equal to
+            // fp16(fp32 x + fp32 b) because binary32 holds the sum of two
+            // binary16 values to within a rounding that cannot move it
+            // across an fp16 rounding boundary (24 >= 2 * 11 + 2).
+            __half2 xh, bh;
+            const uint32_t xw = word(xv, j), bw = word(bv, j);
+            memcpy(&xh, &xw, 4);
+            memcpy(&bh, &bw, 4);
+            const float2 tf = __half22float2(__hadd2(xh, bh));
+            t[2 * j] = tf.x;
+            t[2 * j + 1] = tf.y;
         } else {
-            const float t = __uint_as_float(word(xv, j)) + __uint_as_float(word(bv, j));
-            set_word(out, j, __float_as_uint(gelu_tanh(t)));
+            t[j] = __uint_as_float(word(xv, j)) + __uint_as_float(word(bv, j));
         }
+    }
+    bool far = false;
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+        y[e] = gelu_tanh_fast(t[e]);
+        far |= t[e] < kFarLeft;
+    }
+    if (far) {
+#pragma unroll
+        for (int e = 0; e < kN; ++e)
+            if (t[e] < kFarLeft) y[e] = gelu_tanh_far_left(t[e]);
+    }
+    uint4 out;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (kHalf)
+            set_word(out, j, float2_to_half2(y[2 * j], y[2 * j + 1]));
+        else
+            set_word(out, j, __float_as_uint(y[j]));
     }
     return out;
 }
