@@ -11,10 +11,12 @@ Window (2,6,12), shift (1,3,6).  Inputs are seeded synthetic tensors.
 
 Metric: effective HBM GB/s (algorithmic bytes: each input read once, each
 output written once, plus the index array) and ms per call per kernel.
-Steps run back to back on one stream with a CUDA event between consecutive
-launches, so each kernel owns the interval from the previous launch's end
-mark to its own; one step touches ~1.9 GB (15x the L2), so every input is
-read from HBM and earlier outputs drain to HBM while later kernels run.
+A step's ten launches are captured once, through the public API, in a CUDA
+graph; the graph is replayed K times back to back and CUDA events on the
+launching stream bracket the K replays.  One step touches 1.77 GB (13x the
+L2), so every input is read from HBM and earlier outputs drain to HBM while
+later kernels run.  Per-kernel ms/call comes from each kernel alone,
+replayed back to back over rotating buffer sets.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -296,6 +298,29 @@ def cpu_baseline(calls):
                       f"one step ({nbytes / 1e6:.1f} MB algorithmic, {secs:.2f} s)"}
 
 
+def capture(fn, dev):
+    """Record the launches fn() makes into a CUDA graph (captured on a side
+    stream after one eager warm-up there), so that replays run them back to
+    back with no host work between launches."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    torch.cuda.synchronize(dev)
+    return g
+
+
+def device_sets(calls, dev, n_sets):
+    return [([{k: v.to(dev) for k, v in c.inputs.items()} for c in calls],
+             [{k: torch.empty(sh, dtype=d, device=dev) for k, (sh, d) in c.outputs.items()}
+              for c in calls]) for _ in range(n_sets)]
+
+
 def run_ours(args, rank, world, local):
     import window_gather_swin_gb300 as wgs  # noqa: F401  (loads libwgs.so)
     from window_gather_swin_gb300 import _capi
@@ -311,15 +336,12 @@ def run_ours(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20)
     step_bytes = sum(c.bytes for c in calls)
+    peak, peak_src = measured_hbm_peak()
     # Every input must come from HBM: consecutive uses of one buffer are
     # separated by at least 3x L2 of other traffic.  The full step touches
-    # ~1.9 GB, so one buffer set suffices; a subset (--only) rotates copies.
+    # 1.77 GB, so one buffer set suffices; a subset (--only) rotates copies.
     n_sets = max(1, -(-3 * l2 // step_bytes))
-    sets = []
-    for _ in range(n_sets):
-        sets.append(([{k: v.to(dev) for k, v in c.inputs.items()} for c in calls],
-                     [{k: torch.empty(sh, dtype=d, device=dev) for k, (sh, d) in c.outputs.items()}
-                      for c in calls]))
+    sets = device_sets(calls, dev, n_sets)
     stream = torch.cuda.current_stream(dev)
 
     def step(s, marks=None):
@@ -331,49 +353,63 @@ def run_ours(args, rank, world, local):
             if marks is not None:
                 marks[j + 1].record(stream)
 
+    # One graph per buffer set holds one step: the ten launches, back to back.
+    graphs = [capture(lambda s=s: step(s), dev) for s in range(n_sets)]
     for s in range(args.warmup):  # untimed
-        step(s)
+        graphs[s % n_sets].replay()
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-             for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(smi_id(dev))
     sampler.start()
     barrier(world)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
+    t0.record(stream)
     for s in range(K):
-        step(s, marks[s])
+        graphs[s % n_sets].replay()
+    t1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t_wall
     barrier(world)
     clocks = sampler.stop()
-
-    # kernel j of step s owns the interval between the marks around it
-    per = [[marks[s][j].elapsed_time(marks[s][j + 1]) for s in range(K)] for j in range(len(calls))]
-    region_ms = marks[0][0].elapsed_time(marks[K - 1][len(calls)])
+    region_ms = t0.elapsed_time(t1)
     max_region_ms = reduce_max(region_ms, world, dev)
     all_bytes = reduce_sum(step_bytes * K, world, dev)
     value = all_bytes / (max_region_ms / 1e3) / 1e9
-    peak, peak_src = measured_hbm_peak()
+    del graphs
 
-    kernels = []
-    for c, p in zip(calls, per):
-        mean = statistics.fmean(p)
-        q = sorted(p)
-        gbs = c.bytes / (mean / 1e3) / 1e9
-        kernels.append({"kernel": c.name, "workload": c.workload, "bytes": c.bytes,
-                        "ms_mean": round(mean, 5), "ms_median": round(statistics.median(p), 5),
-                        "ms_min": round(q[0], 5), "ms_p90": round(q[int(0.9 * (len(q) - 1))], 5),
-                        "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
-                        "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)})
-    dom = max(range(len(calls)), key=lambda j: sum(per[j]))
+    # Per kernel, alone: the ms/call figures and the roofline.
+    kernels = run_isolated(calls, dev, l2, peak, args.isolated_launches)
+    dom = max(range(len(calls)), key=lambda j: kernels[j]["ms_per_call"])
     traffic = ncu_traffic().get(calls[dom].label)
     roofline = {"bound": "hbm", "kernel": calls[dom].label,
                 "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(kernels[dom]["gbs"] / peak, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes": calls[dom].bytes}
+
+    # Diagnostic: the same step launched eagerly with an event between
+    # launches, which attributes the step's time to its kernels (each also
+    # drains its predecessor's dirty L2 lines here).
+    in_step = None
+    if not args.no_attribution:
+        ka = min(K, 200)
+        for s in range(3):
+            step(s)
+        marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+                 for _ in range(ka)]
+        torch.cuda.synchronize(dev)
+        for s in range(ka):
+            step(s, marks[s])
+        torch.cuda.synchronize(dev)
+        in_step = []
+        for j, c in enumerate(calls):
+            p = [marks[s][j].elapsed_time(marks[s][j + 1]) for s in range(ka)]
+            in_step.append({"kernel": c.name, "workload": c.workload,
+                            "ms_mean": round(statistics.fmean(p), 5),
+                            "ms_median": round(statistics.median(p), 5)})
+    del sets
 
     e2e = None if args.no_e2e else run_e2e(calls, dev, args, world)
 
@@ -393,11 +429,14 @@ def run_ours(args, rank, world, local):
                    "l2": (f"inputs larger than L2: steps run back to back and one step touches "
                           f"{step_bytes * n_sets / 1e6:.0f} MB over {n_sets} buffer set(s) "
                           f"(L2 {l2 / 1e6:.0f} MB), so every input is read from HBM; no flush"),
-                   "timing": ("CUDA events between consecutive launches on the launching stream; "
-                              "value = all ranks' algorithmic bytes / slowest rank's region time"),
+                   "timing": ("each step's launches are captured once in a CUDA graph through the "
+                              "public API and replayed K times; CUDA events around the K replays on "
+                              "the launching stream; value = all ranks' algorithmic bytes / slowest "
+                              "rank's region time"),
                    "parallelism": f"replicas x{world}"},
         "wall_s": round(wall, 3),
         "kernels": kernels,
+        "kernels_in_step": in_step,
         "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": K * len(calls),
@@ -409,6 +448,41 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_isolated(calls, dev, l2, peak, launches):
+    """Each kernel alone: `per_graph` launches over rotating buffer sets (at
+    least 3x L2 between two uses of a set) captured in one CUDA graph and
+    replayed until about `launches` launches ran.  In this steady state a
+    launch pays for exactly its own traffic, including the write-back of its
+    own previous outputs.  ms per call = region time / launches."""
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for c in calls:
+        n_sets = max(2, -(-3 * l2 // c.bytes))
+        per_graph = max(20, 2 * n_sets)
+        reps = max(1, -(-launches // per_graph))
+        sets = device_sets([c], dev, n_sets)
+        g = capture(lambda: [c.run(sets[s % n_sets][0][0], sets[s % n_sets][1][0])
+                             for s in range(per_graph)], dev)
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        n = reps * per_graph
+        ms = a.elapsed_time(b) / n
+        gbs = c.bytes / (ms / 1e3) / 1e9
+        out.append({"kernel": c.name, "workload": c.workload, "bytes": c.bytes,
+                    "ms_per_call": round(ms, 5), "gbs": round(gbs, 1),
+                    "frac_of_measured": round(gbs / peak, 4),
+                    "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                    "buffer_sets": n_sets, "launches": n})
+        del g, sets
+    return out
 
 
 def smi_id(dev):
@@ -513,12 +587,15 @@ def run_reference(args, rank, world):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--no-attribution", action="store_true",
+                   help="skip the eager per-launch attribution of the step")
+    p.add_argument("--isolated-launches", type=int, default=200)
     p.add_argument("--only", default=None,
                    help="time only the calls whose label contains this text (profiling aid)")
     args = p.parse_args(argv)

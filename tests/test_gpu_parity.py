@@ -365,3 +365,45 @@ def test_python_contract_errors():
     assert wgs.ln_fwd(torch.zeros(0, 192, dtype=torch.float16, device=DEV)).shape == (0, 192)
     assert wgs.bias_gelu_tanh(torch.zeros(0, 8, device=DEV), torch.zeros(8, device=DEV)).shape == (0, 8)
     assert wgs.window_gather(x, torch.zeros(0, dtype=torch.int32, device=DEV)).shape == (0, 192)
+
+
+# ------------------------------------------------------- graph capture ----
+
+def test_identical_results_when_captured_in_a_cuda_graph():
+    """The benchmark replays captured launches; every entry point must give
+    the same bits inside a CUDA graph as eagerly."""
+    st = synth.TINY_PADDED
+    dev = torch.device(DEV)
+    a, b, x, bias = synth.tiny_block(seed=3, stage=st)
+    a, b, x, bias = a.to(dev), b.to(dev), x.to(dev), bias.to(dev)
+    m = window_map(st).to(dev)
+    xl = synth.ln_input(777, 384, seed=9).to(dev)
+
+    def run(outs):
+        wgs.residual_add_ln_fwd(a, b, EPS, residual_out=outs["r"], out=outs["y"])
+        wgs.norm_gather(outs["r"], m, EPS, out=outs["g"])
+        wgs.window_gather(a, m, out=outs["w"])
+        wgs.ln_fwd(xl, EPS, out=outs["l"])
+        wgs.bias_gelu_tanh(x, bias, out=outs["z"])
+
+    def fresh():
+        return {"r": torch.empty_like(a), "y": torch.empty_like(a),
+                "g": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
+                "w": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
+                "l": torch.empty_like(xl), "z": torch.empty_like(x)}
+
+    eager = fresh()
+    run(eager)
+    graphed = fresh()
+    for t in graphed.values():
+        t.fill_(float("nan"))
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        run(graphed)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    for k in eager:
+        assert torch.equal(eager[k].view(torch.uint8), graphed[k].view(torch.uint8)), k

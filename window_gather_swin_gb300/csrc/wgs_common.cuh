@@ -6,8 +6,13 @@
 
 #include <cstdint>
 #include <cstring>
+#include <utility>
 
 #include "wgs.h"
+
+#ifndef WGS_PDL
+#define WGS_PDL 1  // launch with programmatic dependent launch
+#endif
 
 namespace wgs {
 
@@ -22,9 +27,30 @@ struct DeviceInfo {
 };
 wgs_status current_device(DeviceInfo *info);
 
-// Status of the launch just made on this thread.
-inline wgs_status launch_status() {
-    return cudaGetLastError() == cudaSuccess ? WGS_OK : WGS_ERR_LAUNCH;
+// Launch `kernel` on `stream`.  With WGS_PDL the launch allows programmatic
+// dependent launch: the grid may be scheduled while the previous kernel on
+// the stream drains, and every kernel of this library starts with
+// pdl_prologue(), whose griddepcontrol.wait holds it until the previous
+// grid has completed and its writes are visible.  Kernels that do not use
+// these controls (other libraries') keep the usual full serialisation.
+template <typename... Params, typename... Args>
+wgs_status launch(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                  cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = WGS_PDL ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();  // clear this thread's launch error
+        return WGS_ERR_LAUNCH;
+    }
+    return WGS_OK;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -45,6 +71,17 @@ inline bool same_or_disjoint(const void *a, const void *b, int64_t n) {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------- device side --
+
+// First statement of every kernel: wait until the grid launched before this
+// one on the stream has completed (its outputs may be this grid's inputs),
+// then let the next grid start its launch.  Both are no-ops for a launch
+// without programmatic dependent launch.
+__device__ __forceinline__ void pdl_prologue() {
+#if WGS_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
 
 // 16-byte global load that skips L1 (each byte is read exactly once).
 __device__ __forceinline__ uint4 ld_stream(const void *p) {

@@ -125,6 +125,7 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
 template <bool kHalf, int U, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec, int32_t row_vecs) {
+    pdl_prologue();
     constexpr int64_t kTile = static_cast<int64_t>(THREADS) * U;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTile;
     const int32_t in_tile = THREADS % row_vecs;
@@ -158,6 +159,7 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
 template <bool kHalf>
 __global__ void __launch_bounds__(256)
 bias_gelu_scalar_kernel(const void *xp, const void *bp, void *yp, int64_t n, int32_t width) {
+    pdl_prologue();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int32_t c = static_cast<int32_t>(i % width);
@@ -185,17 +187,15 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
         const int64_t n_vec = n / kVec;
         const int64_t need = ceil_div(n_vec, static_cast<int64_t>(T) * U);
         const int64_t cap = static_cast<int64_t>(sm_count) * WGS_GELU_CTAS_PER_SM;
-        bias_gelu_vec_kernel<kHalf, U, T><<<static_cast<unsigned>(need < cap ? need : cap), T, 0,
-                                            stream>>>(static_cast<const uint4 *>(x),
-                                                      static_cast<const uint4 *>(bias),
-                                                      static_cast<uint4 *>(y), n_vec, width / kVec);
-    } else {
-        const int64_t need = ceil_div(n, 256);
-        const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-        bias_gelu_scalar_kernel<kHalf><<<static_cast<unsigned>(need < cap ? need : cap), 256, 0,
-                                         stream>>>(x, bias, y, n, width);
+        return launch(bias_gelu_vec_kernel<kHalf, U, T>,
+                      dim3(static_cast<unsigned>(need < cap ? need : cap)), dim3(T), 0, stream,
+                      static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
+                      static_cast<uint4 *>(y), n_vec, static_cast<int32_t>(width / kVec));
     }
-    return launch_status();
+    const int64_t need = ceil_div(n, 256);
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    return launch(bias_gelu_scalar_kernel<kHalf>, dim3(static_cast<unsigned>(need < cap ? need : cap)),
+                  dim3(256), 0, stream, x, bias, y, n, width);
 }
 
 }  // namespace wgs

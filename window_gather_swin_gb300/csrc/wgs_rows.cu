@@ -48,7 +48,10 @@ struct RowArgs {
 
 template <int WIDTH> struct RowTiling;
 template <> struct RowTiling<192> { static constexpr int kLPR = 8; };
-template <> struct RowTiling<384> { static constexpr int kLPR = 16; };
+#ifndef WGS_LPR384
+#define WGS_LPR384 16  // lanes sharing a 384-wide row
+#endif
+template <> struct RowTiling<384> { static constexpr int kLPR = WGS_LPR384; };
 
 // No-affine LayerNorm of U rows per lane group, each row held as CPL chunks
 // per lane over LPR lanes.  FP32 statistics by the shifted-data two-pass
@@ -56,45 +59,46 @@ template <> struct RowTiling<384> { static constexpr int kLPR = 16; };
 // variance", 1983): with K the row's first element,
 //     m = sum(x - K) / W,  d = (x - K) - m,  var = sum(d^2) / W,
 //     y = fp16(d * (1 / sqrt(var + eps))).
-// Mathematically d = x - mean; numerically the shift keeps the summed terms
-// at the scale of the row's spread instead of its offset, so the rounding
-// error of d no longer grows with |mean|.  Every LN kernel calls this one
-// function, so equal inputs give equal bits.
+// Mathematically d = x - mean; numerically x - K is exact for fp16 inputs
+// and the summed terms stay at the scale of the row's spread instead of its
+// offset, so the error of d no longer grows with |mean|.  Each element is
+// converted to FP32 once and kept in registers; each lane sums its part
+// with four accumulators (short dependency chains), then the LPR lanes of
+// the row combine by butterfly.  Every LN kernel calls this one function,
+// so equal inputs give equal bits.
 template <int WIDTH, int LPR, int CPL, int U>
 __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
+    constexpr int E = CPL * 8;  // elements of one row held by this lane
     const int lead = (threadIdx.x & 31) & ~(LPR - 1);  // lane holding the row's first chunk
-    float shift[U], mean[U], rstd[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-        shift[u] = __shfl_sync(0xffffffffu, half2_to_float2(v[u][0].x).x, lead);
+    float d[U][E];
+    float mean[U], rstd[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float s = 0.f;
+        const float shift = __shfl_sync(0xffffffffu, half2_to_float2(v[u][0].x).x, lead);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < CPL; ++k)
+        for (int c = 0; c < CPL; ++c)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 f = half2_to_float2(word(v[u][k], j));
-                s += f.x - shift[u];
-                s += f.y - shift[u];
+                const float2 f = half2_to_float2(word(v[u][c], j));
+                d[u][c * 8 + 2 * j] = f.x - shift;
+                d[u][c * 8 + 2 * j + 1] = f.y - shift;
+                acc[j] += d[u][c * 8 + 2 * j];
+                acc[j] += d[u][c * 8 + 2 * j + 1];
             }
-        mean[u] = s;
+        mean[u] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) mean[u] = group_sum<LPR>(mean[u]) / static_cast<float>(WIDTH);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float q = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < CPL; ++k)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = half2_to_float2(word(v[u][k], j));
-                const float dx = (f.x - shift[u]) - mean[u], dy = (f.y - shift[u]) - mean[u];
-                q = fmaf(dx, dx, q);
-                q = fmaf(dy, dy, q);
-            }
-        rstd[u] = q;
+        for (int e = 0; e < E; ++e) {
+            d[u][e] -= mean[u];
+            acc[e & 3] = fmaf(d[u][e], d[u][e], acc[e & 3]);
+        }
+        rstd[u] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -104,18 +108,37 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int k = 0; k < CPL; ++k)
+        for (int c = 0; c < CPL; ++c)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = half2_to_float2(word(v[u][k], j));
-                set_word(v[u][k], j,
-                         float2_to_half2(((f.x - shift[u]) - mean[u]) * rstd[u],
-                                         ((f.y - shift[u]) - mean[u]) * rstd[u]));
-            }
+            for (int j = 0; j < 4; ++j)
+                set_word(v[u][c], j,
+                         float2_to_half2(d[u][c * 8 + 2 * j] * rstd[u],
+                                         d[u][c * 8 + 2 * j + 1] * rstd[u]));
+}
+
+// residual_out = fp16(residual + branch) on one 16-byte chunk.  A binary16
+// add rounds the exact sum once, which equals fp16(fp32 a + fp32 b) because
+// binary32 holds the sum closely enough (24 >= 2 * 11 + 2) that the second
+// rounding never crosses an fp16 rounding boundary.
+__device__ __forceinline__ uint4 add_fp16_chunk(const uint4 &a, const uint4 &b) {
+    uint4 r;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __half2 x, y;
+        const uint32_t xa = word(a, j), yb = word(b, j);
+        memcpy(&x, &xa, 4);
+        memcpy(&y, &yb, 4);
+        const __half2 z = __hadd2(x, y);
+        uint32_t zb;
+        memcpy(&zb, &z, 4);
+        set_word(r, j, zb);
+    }
+    return r;
 }
 
 template <RowOp OP, int WIDTH, int U, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
+    pdl_prologue();
     constexpr int LPR = RowTiling<WIDTH>::kLPR;
     constexpr int CPL = WIDTH / 8 / LPR;
     constexpr int RPW = 32 / LPR;                 // rows per warp per group
@@ -171,13 +194,7 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
-                for (int k = 0; k < CPL; ++k)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 x = half2_to_float2(word(v[u][k], j));
-                        const float2 y = half2_to_float2(word(b[u][k], j));
-                        set_word(v[u][k], j, float2_to_half2(x.x + y.x, x.y + y.y));
-                    }
+                for (int k = 0; k < CPL; ++k) v[u][k] = add_fp16_chunk(v[u][k], b[u][k]);
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (live[u])
@@ -203,6 +220,7 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
 __global__ void __launch_bounds__(256) gather_any_width_kernel(const uint4 *src, const int32_t *idx,
                                                                 uint4 *dst, int64_t n_src,
                                                                 int64_t n_idx, int32_t chunks) {
+    pdl_prologue();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t d = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -226,8 +244,7 @@ wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     const int64_t iters = ceil_div(a.rows, ROWS_CTA);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
     const unsigned grid = static_cast<unsigned>(iters < cap ? iters : cap);
-    row_kernel<OP, WIDTH, U, WARPS><<<grid, WARPS * 32, 0, stream>>>(a);
-    return launch_status();
+    return launch(row_kernel<OP, WIDTH, U, WARPS>, dim3(grid), dim3(WARPS * 32), 0, stream, a);
 }
 
 template <RowOp OP>
@@ -309,9 +326,9 @@ extern "C" wgs_status window_gather(const void *src, const int32_t *idx, void *d
     const int64_t warps_needed = n_idx;
     const int64_t blocks = ceil_div(warps_needed, 8);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
-    gather_any_width_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
-        static_cast<const uint4 *>(src), idx, static_cast<uint4 *>(dst), n_src, n_idx, width / 8);
-    return launch_status();
+    return launch(gather_any_width_kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)),
+                  dim3(256), 0, stream, static_cast<const uint4 *>(src), idx,
+                  static_cast<uint4 *>(dst), n_src, n_idx, static_cast<int32_t>(width / 8));
 }
 
 extern "C" wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
