@@ -157,30 +157,39 @@ def measured_hbm_peak():
 def ncu_traffic():
     """dram bytes per launch from ncu captures, keyed by kernel label.  Each
     line of profiles/ncu_traffic.txt is `label | sources digest | bytes`; a
-    figure counts only while the kernel sources still hash to its digest."""
+    figure counts only while the sources of that kernel still hash to its
+    digest (see sources_digest)."""
     out = {}
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return out
-    digest = sources_digest()
     with open(path) as f:
         for line in f:
             line = line.split("#", 1)[0].strip()
             if line.count("|") != 2:
                 continue
             label, sha, nbytes = (p.strip() for p in line.split("|"))
-            if sha == digest:
+            if sha == sources_digest(label):
                 out[label] = float(nbytes)
     return out
 
 
-def sources_digest():
+KERNEL_SOURCES = {
+    "bias_gelu_tanh": ["window_gather_swin_gb300/csrc/wgs_gelu.cu"],
+    "": ["window_gather_swin_gb300/csrc/wgs_rows.cu"],  # LN, add + LN, gathers
+}
+
+
+def sources_digest(label: str) -> str:
+    """Hash of the files that define the kernel behind `label`: its .cu file,
+    the shared device header and the C ABI header."""
     import hashlib
+    own = next(v for k, v in KERNEL_SOURCES.items() if label.startswith(k))
+    files = own + ["window_gather_swin_gb300/csrc/wgs_common.cuh", "include/wgs.h"]
     h = hashlib.sha256()
-    for d in (os.path.join(ROOT, "window_gather_swin_gb300", "csrc"), os.path.join(ROOT, "include")):
-        for name in sorted(os.listdir(d)):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for rel in files:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

@@ -15,8 +15,6 @@
 // store; the statistics use the shifted-data two-pass method (see
 // ln_normalize).  Each warp works on U row groups at once so that every lane has
 // U * CPL independent 16-byte loads in flight before its first reduction.
-#include <atomic>
-
 #include "wgs_common.cuh"
 
 #ifndef WGS_ROW_WARPS
@@ -27,9 +25,6 @@
 #endif
 #ifndef WGS_ROW_CTAS_PER_SM
 #define WGS_ROW_CTAS_PER_SM 64  // grid cap, in CTAs per SM (grid-stride beyond it)
-#endif
-#ifndef WGS_ROW_IMPL
-#define WGS_ROW_IMPL 0  // 0: one pass per CTA, 2: persistent software-pipelined warps
 #endif
 
 namespace wgs {
@@ -225,96 +220,6 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
     }
 }
 
-// Persistent form: one resident wave of CTAs; warp w of the grid takes row
-// groups w, w + W, w + 2W, ... (W = warps in the grid) and keeps the next
-// group's loads in flight while it normalises and stores the current one.
-// Gathers run a third stage ahead: the index of the group after next is
-// loaded one iteration early, so the dependent row load never stalls the
-// group being processed.  All SMs then stream until the last group, and
-// the grid ends within one group's time of itself.
-template <RowOp OP, int WIDTH, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) row_persist_kernel(const RowArgs a) {
-    pdl_prologue();
-    constexpr int LPR = RowTiling<WIDTH>::kLPR;
-    constexpr int CPL = WIDTH / 8 / LPR;
-    constexpr int RPW = 32 / LPR;
-    constexpr bool kGatherOp = OP == RowOp::kGather || OP == RowOp::kNormGather;
-    constexpr bool kNorm = OP != RowOp::kGather;
-    constexpr int NB = OP == RowOp::kAddLN ? 2 : 1;  // input tensors
-    const int lane = threadIdx.x & 31;
-    const int grp = lane / LPR, sub = lane % LPR;
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const int64_t groups = (a.rows + RPW - 1) / RPW;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * WARPS;
-    int64_t g = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
-
-    // source row of group gi for this lane group (-1: pad, bad index or past the end)
-    auto source = [&](int64_t gi, bool &live) -> int64_t {
-        const int64_t row = gi * RPW + grp;
-        live = gi < groups && row < a.rows;
-        if constexpr (kGatherOp) {
-            if (!live) return -1;
-            const int32_t s = __ldg(a.idx + row);
-            const bool ok = s >= 0 && s < a.n_src;
-            if (!ok && s != -1 && sub == 0) atomicOr(&g_index_error, 1u);
-            return ok ? s : -1;
-        } else {
-            return live ? row : -1;
-        }
-    };
-    auto fetch = [&](int64_t src, int64_t row, uint4 (&v)[NB][CPL]) {
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            v[0][k] = src >= 0 ? ld_stream(a.in0 + src * WIDTH + (sub + k * LPR) * 8) : zero;
-            if constexpr (NB == 2)
-                v[1][k] = src >= 0 ? ld_stream(a.in1 + row * WIDTH + (sub + k * LPR) * 8) : zero;
-        }
-    };
-
-    bool live0, live1;
-    int64_t src0 = source(g, live0);
-    int64_t src1 = source(g + step, live1);
-    uint4 cur[NB][CPL];
-    fetch(src0, g * RPW + grp, cur);
-    while (g < groups) {
-        const int64_t row = g * RPW + grp;
-        const bool live = live0;
-        const bool valid = src0 >= 0;
-        uint4 nxt[NB][CPL];
-        fetch(src1, (g + step) * RPW + grp, nxt);
-        bool live2;
-        const int64_t src2 = source(g + 2 * step, live2);
-
-        uint4 v[1][CPL];
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) v[0][k] = cur[0][k];
-        if constexpr (OP == RowOp::kAddLN) {
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) v[0][k] = add_fp16_chunk(v[0][k], cur[1][k]);
-            if (live)
-#pragma unroll
-                for (int k = 0; k < CPL; ++k)
-                    st_stream(a.out0 + row * WIDTH + (sub + k * LPR) * 8, v[0][k]);
-        }
-        if constexpr (kNorm) ln_normalize<WIDTH, LPR, CPL, 1>(v, a.eps);
-        __half *out = OP == RowOp::kAddLN ? a.out1 : a.out0;
-        if (live)
-#pragma unroll
-            for (int k = 0; k < CPL; ++k)
-                st_stream(out + row * WIDTH + (sub + k * LPR) * 8, valid ? v[0][k] : zero);
-
-#pragma unroll
-        for (int n = 0; n < NB; ++n)
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) cur[n][k] = nxt[n][k];
-        g += step;
-        src0 = src1;
-        live0 = live1;
-        src1 = src2;
-        live1 = live2;
-    }
-}
-
 // Gather for any width that is a whole number of 16-byte chunks: one warp
 // per destination row, lanes striding over the row's chunks.
 __global__ void __launch_bounds__(256) gather_any_width_kernel(const uint4 *src, const int32_t *idx,
@@ -339,31 +244,12 @@ wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     DeviceInfo dev;
     const wgs_status st = current_device(&dev);
     if (st != WGS_OK) return st;
-#if WGS_ROW_IMPL == 2
-    constexpr int WARPS = WGS_ROW_WARPS;
-    auto kernel = row_persist_kernel<OP, WIDTH, WARPS>;
-    static std::atomic<int> ctas_per_sm[64];  // per device, for this instantiation
-    int per_sm = ctas_per_sm[dev.device].load(std::memory_order_relaxed);
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, WARPS * 32, 0) !=
-                cudaSuccess ||
-            per_sm < 1)
-            return WGS_ERR_LAUNCH;
-        ctas_per_sm[dev.device].store(per_sm, std::memory_order_relaxed);
-    }
-    const int64_t groups = ceil_div(a.rows, 32 / RowTiling<WIDTH>::kLPR);
-    int64_t grid = static_cast<int64_t>(per_sm) * dev.sm_count;
-    const int64_t need = ceil_div(groups, WARPS);
-    if (grid > need) grid = need;
-    return launch(kernel, dim3(static_cast<unsigned>(grid)), dim3(WARPS * 32), 0, stream, a);
-#else
     constexpr int U = WGS_ROW_U, WARPS = WGS_ROW_WARPS;
     constexpr int ROWS_CTA = WARPS * (32 / RowTiling<WIDTH>::kLPR) * U;
     const int64_t iters = ceil_div(a.rows, ROWS_CTA);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
     const unsigned grid = static_cast<unsigned>(iters < cap ? iters : cap);
     return launch(row_kernel<OP, WIDTH, U, WARPS>, dim3(grid), dim3(WARPS * 32), 0, stream, a);
-#endif
 }
 
 template <RowOp OP>
