@@ -40,6 +40,9 @@ def _load():
             "orc_build_window_index": (ctypes.c_int, [P, P, P, P, i32, P]),
             "orc_window_gather": (i64, [P, P, P, i64, i64, i32]),
             "orc_norm_gather": (i64, [P, P, P, i64, i64, i32, f32]),
+            "orc_window_reverse_add_ln": (i64, [P, P, P, P, P, i64, i64, i32, f32]),
+            "orc_invert_window_index": (None, [P, i64, P, i64]),
+            "orc_residual_add_norm_gather": (i64, [P, P, P, P, P, i64, i64, i32, f32]),
             "orc_bias_gelu_f32": (None, [P, P, P, P, i64, i32]),
             "orc_bias_gelu_f16": (None, [P, P, P, P, i64, i32]),
         }
@@ -159,6 +162,44 @@ def norm_gather(src, idx, eps: float = 1e-5):
     dst = np.empty((i.size, s.shape[1]), dtype=np.float16)
     bad = _load().orc_norm_gather(_ptr(s), _ptr(i), _ptr(dst), s.shape[0], i.size, s.shape[1], eps)
     return dst, int(bad)
+
+
+# ------------------------------------------------ block-boundary fusions ----
+
+def window_reverse_add_ln(residual, attn, idx, eps: float = 1e-5):
+    """Returns (residual_out, y, anomalies): r[t] = fp16(residual[t] + attn[d])
+    for the windowed row d with idx[d] == t, y = LN(r)."""
+    r = _c(residual, np.float16)
+    w = _c(attn, np.float16)
+    i = _c(idx, np.int32).ravel()
+    assert r.ndim == 2 and w.ndim == 2 and r.shape[1] == w.shape[1] and w.shape[0] == i.size
+    r_out = np.empty_like(r)
+    y = np.empty_like(r)
+    bad = _load().orc_window_reverse_add_ln(_ptr(r), _ptr(w), _ptr(i), _ptr(r_out), _ptr(y),
+                                            r.shape[0], i.size, r.shape[1], eps)
+    return r_out, y, int(bad)
+
+
+def invert_window_index(idx, n_tokens: int) -> np.ndarray:
+    """inv[t] = the windowed row that names token t (-1 if none)."""
+    i = _c(idx, np.int32).ravel()
+    inv = np.empty(n_tokens, dtype=np.int32)
+    _load().orc_invert_window_index(_ptr(i), i.size, _ptr(inv), n_tokens)
+    return inv
+
+
+def residual_add_norm_gather(residual, branch, idx, eps: float = 1e-5):
+    """Returns (residual_out, dst, bad): r = fp16(residual + branch),
+    dst[d] = LN(r)[idx[d]] (zero row for -1)."""
+    a = _c(residual, np.float16)
+    b = _c(branch, np.float16)
+    i = _c(idx, np.int32).ravel()
+    assert a.shape == b.shape and a.ndim == 2
+    r = np.empty_like(a)
+    dst = np.empty((i.size, a.shape[1]), dtype=np.float16)
+    bad = _load().orc_residual_add_norm_gather(_ptr(a), _ptr(b), _ptr(i), _ptr(r), _ptr(dst),
+                                               a.shape[0], i.size, a.shape[1], eps)
+    return r, dst, int(bad)
 
 
 # ---------------------------------------------------------------- GELU ----

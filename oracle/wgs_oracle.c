@@ -352,3 +352,68 @@ void orc_bias_gelu_f16(const uint16_t *x, const uint16_t *bias, uint16_t *y, dou
             if (y) y[i] = orc_rn16(g);
         }
 }
+
+/* ------------------------------------------------------------------ */
+/* Window reverse fused with residual add + LN                         */
+/* ------------------------------------------------------------------ */
+/* [P1 s7] keeps a "restore path" custom op; [P1 s1] counts two
+ * index_select calls per block (32 over 16 blocks).  The plainest reading:
+ * after window attention the windowed rows go back to token order (the
+ * inverse of the s5 gather: crop pads, undo the window order and the cyclic
+ * shift), are added to the residual stream and normalised (norm2), keeping
+ * the s4 rounding point:
+ *     r[t] = fp16(residual[t] + attn[d])  for the windowed row d with idx[d] = t
+ *     y[t] = LN(r[t])
+ * It is written here as a scatter through the forward map idx.  A token
+ * that no windowed row names takes a zero branch (r = residual) and is
+ * counted, as is a token named more than once (the last row wins).
+ * Returns that count (0 for any map from orc_build_window_index). */
+int64_t orc_window_reverse_add_ln(const uint16_t *residual, const uint16_t *attn,
+                                  const int32_t *idx, uint16_t *r_out, uint16_t *y,
+                                  int64_t n_tokens, int64_t n_idx, int32_t width, float eps)
+{
+    int32_t *seen = (int32_t *)calloc((size_t)(n_tokens > 0 ? n_tokens : 1), sizeof(int32_t));
+    for (int64_t t = 0; t < n_tokens * (int64_t)width; ++t) r_out[t] = residual[t];
+    for (int64_t d = 0; d < n_idx; ++d) {
+        int64_t t = idx[d];
+        if (t < 0 || t >= n_tokens) continue;
+        seen[t] += 1;
+        for (int32_t i = 0; i < width; ++i) {
+            int64_t k = t * (int64_t)width + i;
+            r_out[k] = orc_rn16(orc_f16_to_f64(residual[k]) + orc_f16_to_f64(attn[d * (int64_t)width + i]));
+        }
+    }
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n_tokens; ++t) bad += seen[t] != 1;
+    free(seen);
+    orc_ln(r_out, y, n_tokens, width, eps);
+    return bad;
+}
+
+/* token -> windowed row: inv[idx[d]] = d; tokens no row names get -1 */
+void orc_invert_window_index(const int32_t *idx, int64_t n_idx, int32_t *inv, int64_t n_tokens)
+{
+    for (int64_t t = 0; t < n_tokens; ++t) inv[t] = -1;
+    for (int64_t d = 0; d < n_idx; ++d)
+        if (idx[d] >= 0 && idx[d] < n_tokens) inv[idx[d]] = (int32_t)d;
+}
+
+/* ------------------------------------------------------------------ */
+/* Residual add + norm1 + shifted-window gather                        */
+/* ------------------------------------------------------------------ */
+/* The block boundary: the residual stream r = fp16(a + b) is written out
+ * ([P1 s4]) and the next block's norm1 output is consumed only by its
+ * window gather ([P1 s5]), so
+ *     r = fp16(a + b),   dst[d] = LN(r)[idx[d]]  (zero row for -1).
+ * Written as the composition of the two definitions above.  Returns the
+ * number of indices outside [-1, n_src). */
+int64_t orc_residual_add_norm_gather(const uint16_t *a, const uint16_t *b, const int32_t *idx,
+                                     uint16_t *r_out, uint16_t *dst, int64_t n_src,
+                                     int64_t n_idx, int32_t width, float eps)
+{
+    uint16_t *y = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(n_src * (int64_t)width + 1));
+    orc_residual_add_ln(a, b, r_out, y, n_src, width, eps);
+    int64_t bad = orc_window_gather(y, idx, dst, n_src, n_idx, width);
+    free(y);
+    return bad;
+}

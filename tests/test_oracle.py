@@ -407,3 +407,70 @@ def test_parity_rules_accept_fp32_rounding_and_reject_real_errors():
     check_ln(_ln_fp32_shifted(xs), ys16, ys64, "small variance")
     with pytest.raises(AssertionError):
         check_ln(_ln_fp32_shifted(xs, drop_eps=True), ys16, ys64, "eps dropped")
+
+
+# --------------------------------------------- block-boundary fusions ----
+
+REV_CASES = [(synth.TINY, None, 0), (synth.TINY_PADDED, None, 0), (synth.TINY_PADDED, None, 1),
+             (synth.STAGE_384, synth.STAGE_384.padded, 0)]
+
+
+@pytest.mark.parametrize("stage,padded,flags", REV_CASES)
+def test_window_reverse_undoes_the_window_gather(stage, padded, flags):
+    m = oracle.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, padded, flags)
+    x = synth.gather_source(stage.tokens, 64, seed=5).numpy()
+    windows, _ = oracle.window_gather(x, m)
+    r, _, bad = oracle.window_reverse_add_ln(np.zeros_like(x), windows, m)
+    assert bad == 0
+    assert np.array_equal(r.view(np.uint16), x.view(np.uint16))
+
+
+@pytest.mark.parametrize("stage,padded,flags", REV_CASES[:3])
+def test_window_reverse_add_ln_matches_numpy_composition(stage, padded, flags):
+    m = oracle.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, padded, flags)
+    res, _ = synth.residual_branch(stage.tokens, 192, seed=6)
+    res = res.numpy()
+    attn = synth.gather_source(m.size, 192, seed=7).numpy() * np.float16(0.1)
+    r, y, bad = oracle.window_reverse_add_ln(res, attn, m, EPS)
+    assert bad == 0
+    # independent: numpy's own inverse by fancy assignment and its float16 add
+    inv = np.full(stage.tokens, -1, dtype=np.int64)
+    inv[m[m >= 0]] = np.nonzero(m >= 0)[0]
+    want = res + attn[inv]
+    assert np.array_equal(r.view(np.uint16), want.view(np.uint16))
+    assert np.array_equal(y.view(np.uint16), oracle.ln(want, EPS).view(np.uint16))
+
+
+def test_window_reverse_counts_uncovered_tokens():
+    m = oracle.build_window_index(synth.TINY.grid, synth.WINDOW, synth.SHIFT)
+    m2 = m.copy()
+    lost = m2[5]
+    m2[5] = -1
+    res = synth.gather_source(synth.TINY.tokens, 64, seed=1).numpy()
+    attn = synth.gather_source(m.size, 64, seed=2).numpy()
+    r, _, bad = oracle.window_reverse_add_ln(res, attn, m2)
+    assert bad == 1
+    assert np.array_equal(r[lost].view(np.uint16), res[lost].view(np.uint16))
+
+
+def test_invert_window_index():
+    st = synth.TINY_PADDED
+    m = oracle.build_window_index(st.grid, synth.WINDOW, synth.SHIFT)
+    inv = oracle.invert_window_index(m, st.tokens)
+    assert (inv >= 0).all()
+    assert np.array_equal(m[inv], np.arange(st.tokens))
+    assert np.array_equal(np.sort(inv), np.nonzero(m >= 0)[0])
+
+
+def test_residual_add_norm_gather_matches_numpy_composition():
+    st = synth.TINY_PADDED
+    m = oracle.build_window_index(st.grid, synth.WINDOW, synth.SHIFT)
+    a, b = synth.residual_branch(st.tokens, 192, seed=8)
+    a, b = a.numpy(), b.numpy()
+    r, dst, bad = oracle.residual_add_norm_gather(a, b, m, EPS)
+    assert bad == 0
+    want_r = a + b  # numpy float16 add: fp16(fp32 a + fp32 b)
+    assert np.array_equal(r.view(np.uint16), want_r.view(np.uint16))
+    ln = oracle.ln(want_r, EPS)
+    want = np.where((m >= 0)[:, None], ln[np.maximum(m, 0)], np.float16(0))
+    assert np.array_equal(dst.view(np.uint16), want.view(np.uint16))
