@@ -122,6 +122,35 @@ def build_calls():
     return calls
 
 
+def build_next_calls():
+    """The block-boundary fusions beyond the step (window reverse + residual
+    add + LN; residual add + norm1 + window gather), at both stages."""
+    import window_gather_swin_gb300 as wgs
+    calls = []
+    for st in (synth.STAGE_192, synth.STAGE_384):
+        n, c = st.tokens, st.width
+        idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+        inv = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+        m = idx.numel()
+        res, br = synth.residual_branch(n, c, seed=2)
+        windows = synth.gather_source(m, c, seed=3)
+        calls.append(Call(
+            "window_reverse_add_ln_fwd", f"{m}->[{n},{c}]", 8 * n * c + 4 * n,
+            {"res": res, "win": windows, "inv": inv},
+            {"r": ((n, c), torch.float16), "y": ((n, c), torch.float16)},
+            lambda i, o: wgs.window_reverse_add_ln_fwd(i["res"], i["win"], i["inv"], EPS,
+                                                       residual_out=o["r"], out=o["y"]),
+            None, n))
+        calls.append(Call(
+            "residual_add_norm_gather", f"[{n},{c}]->{m}", 6 * n * c + (2 * c + 4) * m,
+            {"a": res, "b": br, "idx": idx},
+            {"r": ((n, c), torch.float16), "dst": ((m, c), torch.float16)},
+            lambda i, o: wgs.residual_add_norm_gather(i["a"], i["b"], i["idx"], EPS,
+                                                      residual_out=o["r"], out=o["dst"]),
+            None, m))
+    return calls
+
+
 def _k(n, f):
     return max(1, int(n * f))
 
@@ -398,6 +427,10 @@ def run_ours(args, rank, world, local):
                 "frac": round(kernels[dom]["gbs"] / peak, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes": calls[dom].bytes}
 
+    kernels_next = None
+    if not args.only:
+        kernels_next = run_isolated(build_next_calls(), dev, l2, peak, args.isolated_launches)
+
     # Diagnostic: the same step launched eagerly with an event between
     # launches, which attributes the step's time to its kernels (each also
     # drains its predecessor's dirty L2 lines here).
@@ -446,6 +479,7 @@ def run_ours(args, rank, world, local):
         "wall_s": round(wall, 3),
         "kernels": kernels,
         "kernels_in_step": in_step,
+        "kernels_next": kernels_next,
         "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": K * len(calls),

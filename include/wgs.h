@@ -135,6 +135,55 @@ wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n
                        int64_t n_idx, int32_t width, float eps, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* window_reverse_add_ln_fwd -- window reverse + residual add + LN     */
+/*                                          [P1 s5 inverse, s4, s7]    */
+/* ------------------------------------------------------------------ */
+/* After window attention the windowed rows return to token order (the
+ * inverse of window_gather: crop pads, undo the window order and the
+ * cyclic shift), join the residual stream and feed norm2, in one pass.
+ * P1 s7 keeps such a "restore path" op; s4 fixes the rounding point:
+ *     residual_out[t] = fp16(fp32(residual[t]) + fp32(windows[inv_idx[t]]))
+ *     y[t]            = LN(residual_out[t])                   (as ln_fwd)
+ *   residual, residual_out, y  fp16 [rows, width], 16-byte aligned;
+ *          residual_out and y may each equal residual, must differ from
+ *          each other; other overlaps return WGS_ERR_ALIAS.
+ *   windows  fp16 [n_windowed, width], 16-byte aligned, read at the rows
+ *          inv_idx names; must not overlap the outputs.
+ *   inv_idx  int32 [rows]: the windowed row of each token, usually from
+ *          wgs_build_window_inverse.  A value outside [0, n_windowed) sets
+ *          the device error word and that token takes no branch
+ *          (residual_out = residual, bit for bit).
+ *   width  192 or 384 only. */
+wgs_status window_reverse_add_ln_fwd(const void *residual, const void *windows,
+                                     const int32_t *inv_idx, void *residual_out, void *y,
+                                     int64_t rows, int64_t n_windowed, int32_t width, float eps,
+                                     cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* residual_add_norm_gather -- residual add + norm1 + window gather    */
+/*                                                  [P1 s4, s5]        */
+/* ------------------------------------------------------------------ */
+/* At a block boundary the residual stream is updated and written out (s4)
+ * and the next block's norm1 output is consumed only by its window gather
+ * (s5); one pass does all three:
+ *     residual_out[s] = fp16(fp32(residual[s]) + fp32(branch[s]))
+ *     dst[d]          = LN(residual_out[idx[d]])   (zero row for -1)
+ * Equal, bit for bit, to residual_add_ln_fwd followed by window_gather of
+ * its y.  Each source row s is processed by the destination row that names
+ * it: rows of residual_out that idx never names are NOT written (a map from
+ * wgs_build_window_index names every token exactly once).
+ *   residual, branch, residual_out  fp16 [n_src, width], 16-byte aligned;
+ *          residual_out may equal residual or branch (in place is exact
+ *          only when idx names each row at most once).
+ *   dst    fp16 [n_idx, width], must not overlap anything else.
+ *   idx    int32 [n_idx], as for window_gather (bad values: zero row and
+ *          the device error word).
+ *   width  192 or 384 only. */
+wgs_status residual_add_norm_gather(const void *residual, const void *branch, const int32_t *idx,
+                                    void *residual_out, void *dst, int64_t n_src, int64_t n_idx,
+                                    int32_t width, float eps, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* bias_gelu_tanh -- fused bias + tanh-approximate GELU       [P3 s3] */
 /* ------------------------------------------------------------------ */
 /*     t = x + bias[col]   (rounded once to the tensor dtype)
@@ -180,6 +229,14 @@ int64_t wgs_window_index_count(const int32_t grid[3], const int32_t window[3],
 wgs_status wgs_build_window_index(const int32_t grid[3], const int32_t window[3],
                                   const int32_t shift[3], const int32_t *padded, int32_t flags,
                                   int32_t *out_host, int64_t out_len);
+
+/* Fill inv_host[0 .. grid[0]*grid[1]*grid[2]) with the inverse map: the
+ * windowed row that holds each token (same arguments as
+ * wgs_build_window_index; out_len must be at least the token count, else
+ * WGS_ERR_SHAPE).  Host memory only; no CUDA call is made. */
+wgs_status wgs_build_window_inverse(const int32_t grid[3], const int32_t window[3],
+                                    const int32_t shift[3], const int32_t *padded, int32_t flags,
+                                    int32_t *inv_host, int64_t out_len);
 
 /* Read and clear the current device's index error word after the work
  * already queued on `stream` has finished.  This call synchronises

@@ -171,3 +171,52 @@ def test_python_rejects_cpu_and_bad_tensors():
         wgs.window_gather(x, torch.zeros(3, dtype=torch.int32))
     with pytest.raises(RuntimeError):
         wgs.build_window_index((2, 12, 24), (2, 6, 12), (1, 3, 6), padded=(2, 11, 24))
+
+
+# --------------------------------------------------- inverse index map ----
+
+@pytest.mark.parametrize("grid,padded,flags", CASES)
+def test_library_inverse_map_equals_inverted_oracle_map(grid, padded, flags):
+    got = wgs.build_window_inverse(grid, synth.WINDOW, synth.SHIFT, padded, flags).numpy()
+    fwd = oracle.build_window_index(grid, synth.WINDOW, synth.SHIFT, padded, flags)
+    want = oracle.invert_window_index(fwd, int(np.prod(grid)))
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("shift", [(0, 0, 0), (-1, -3, -6), (9, 100, -250)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_library_inverse_map_odd_shifts(shift, flags):
+    grid, win = (3, 7, 10), (2, 3, 4)
+    got = wgs.build_window_inverse(grid, win, shift, None, flags).numpy()
+    fwd = oracle.build_window_index(grid, win, shift, None, flags)
+    assert np.array_equal(got, oracle.invert_window_index(fwd, 210))
+
+
+def test_inverse_builder_errors(lib):
+    g = (ctypes.c_int32 * 3)(2, 12, 24)
+    w = (ctypes.c_int32 * 3)(2, 6, 12)
+    s = (ctypes.c_int32 * 3)(1, 3, 6)
+    out = (ctypes.c_int32 * 576)()
+    assert lib.wgs_build_window_inverse(g, w, s, None, 0, out, 575) == SHAPE
+    assert lib.wgs_build_window_inverse(g, w, s, None, 3, out, 576) == SHAPE
+    assert lib.wgs_build_window_inverse(g, w, None, None, 0, out, 576) == NULL
+    assert lib.wgs_build_window_inverse(g, w, s, None, 0, out, 576) == OK
+
+
+def test_block_boundary_argument_errors(lib):
+    rev = lib.window_reverse_add_ln_fwd
+    assert rev(A, B, C, D, A + 2 ** 20, 10, 12, 256, 1e-5, None) == WIDTH
+    assert rev(A, B, C, D, A + 2 ** 20, -1, 12, 192, 1e-5, None) == SHAPE
+    assert rev(None, None, None, None, None, 0, 12, 192, 1e-5, None) == OK
+    assert rev(A, B, None, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == NULL
+    assert rev(A, B, C + 2, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIGN
+    assert rev(A, B, C, D, D, 10, 12, 192, 1e-5, None) == ALIAS          # r == y
+    assert rev(A, D + 384, C, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIAS  # windows in r
+    ang = lib.residual_add_norm_gather
+    assert ang(A, B, C, D, A + 2 ** 20, 10, 12, 100, 1e-5, None) == WIDTH
+    assert ang(A, B, C, D, A + 2 ** 20, 10, -1, 192, 1e-5, None) == SHAPE
+    assert ang(None, None, C, None, D, 10, 0, 192, 1e-5, None) == OK
+    assert ang(A, None, C, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == NULL
+    assert ang(A, B, C + 1, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIGN
+    assert ang(A, B, C, D, D + 128, 10, 12, 192, 1e-5, None) == ALIAS    # dst inside r
+    assert ang(A, B, C, A + 768, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIAS  # shifted r

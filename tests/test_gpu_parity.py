@@ -230,6 +230,108 @@ def test_gather_all_pads_and_empty_source():
     assert not np_(dst).view(np.uint16).any()
 
 
+# --------------------------------------------- block-boundary fusions ----
+
+def _reverse_case(stage, padded="stage", flags=0, seed=11):
+    p = stage.padded if padded == "stage" else padded
+    m = oracle.build_window_index(stage.grid, synth.WINDOW, synth.SHIFT, p, flags)
+    inv = wgs.build_window_inverse(stage.grid, synth.WINDOW, synth.SHIFT, p, flags)
+    res, _ = synth.residual_branch(stage.tokens, stage.width, seed=seed)
+    windows = synth.gather_source(m.size, stage.width, seed=seed + 1)
+    return m, inv, res, windows
+
+
+@pytest.mark.parametrize("stage,flags", [(synth.TINY, 0), (synth.TINY_PADDED, 0),
+                                         (synth.TINY_PADDED, 1), (synth.STAGE_192, 0),
+                                         (synth.STAGE_384, 0)],
+                         ids=["tiny", "tiny_padded", "tiny_padded_pts", "c192", "c384"])
+def test_window_reverse_add_ln(stage, flags):
+    m, inv, res, windows = _reverse_case(stage, flags=flags)
+    r, y = wgs.window_reverse_add_ln_fwd(res.to(DEV), windows.to(DEV), inv.to(DEV), EPS)
+    o_r, o_y, bad = oracle.window_reverse_add_ln(res.numpy(), windows.numpy(), m, EPS)
+    assert bad == 0
+    assert_bitwise(np_(r), o_r, "residual_out")
+    st = check_ln(np_(y), o_y, oracle.ln_f64(o_r, EPS), "reverse add+ln")
+    print("reverse add+ln", stage.name, st)
+    wgs.check_error(DEV)
+
+
+@pytest.mark.parametrize("stage", [synth.TINY, synth.TINY_PADDED, synth.STAGE_192, synth.STAGE_384],
+                         ids=lambda s: s.name)
+def test_residual_add_norm_gather(stage):
+    m = window_map(stage)
+    om = oracle_map(stage)
+    a, b = synth.residual_branch(stage.tokens, stage.width, seed=12)
+    r, dst = wgs.residual_add_norm_gather(a.to(DEV), b.to(DEV), m.to(DEV), EPS)
+    o_r, o_dst, bad = oracle.residual_add_norm_gather(a.numpy(), b.numpy(), om, EPS)
+    assert bad == 0
+    assert_bitwise(np_(r), o_r, "residual_out")
+    y64 = oracle.ln_f64(o_r, EPS)
+    want64 = np.where((om >= 0)[:, None], y64[np.maximum(om, 0)], 0.0)
+    g = np_(dst)
+    assert_bitwise(g[om < 0], o_dst[om < 0], "pad rows")
+    st = check_ln(g, o_dst, want64, "add+norm+gather")
+    print("add+norm+gather", stage.name, st)
+
+
+def test_block_boundary_identities():
+    """The fused ops equal their unfused compositions bit for bit, and the
+    reverse undoes the gather."""
+    st = synth.STAGE_384
+    dev = torch.device(DEV)
+    m = window_map(st).to(dev)
+    inv = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT, st.padded).to(dev)
+    a, b = synth.residual_branch(st.tokens, st.width, seed=13)
+    a, b = a.to(dev), b.to(dev)
+    r, dst = wgs.residual_add_norm_gather(a, b, m, EPS)
+    r2, y2 = wgs.residual_add_ln_fwd(a, b, EPS)
+    assert torch.equal(r.view(torch.int16), r2.view(torch.int16))
+    assert torch.equal(dst.view(torch.int16), wgs.window_gather(y2, m).view(torch.int16))
+    windows = synth.gather_source(m.numel(), st.width, seed=14).to(dev)
+    rr, yy = wgs.window_reverse_add_ln_fwd(a, windows, inv, EPS)
+    unwindowed = windows[inv.long()]
+    r3, y3 = wgs.residual_add_ln_fwd(a, unwindowed, EPS)
+    assert torch.equal(rr.view(torch.int16), r3.view(torch.int16))
+    assert torch.equal(yy.view(torch.int16), y3.view(torch.int16))
+    # round trip: tokens -> windows -> tokens over a zero residual
+    x = synth.gather_source(st.tokens, st.width, seed=15).to(dev)
+    back, _ = wgs.window_reverse_add_ln_fwd(torch.zeros_like(x), wgs.window_gather(x, m), inv, EPS)
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))
+
+
+def test_window_reverse_bad_inverse_index_keeps_residual():
+    wgs.check_error(DEV)
+    st = synth.TINY
+    _, inv, res, windows = _reverse_case(st)
+    inv = inv.clone()
+    inv[3] = -1
+    inv[7] = windows.shape[0]
+    r, _ = wgs.window_reverse_add_ln_fwd(res.to(DEV), windows.to(DEV), inv.to(DEV), EPS)
+    assert np.array_equal(np_(r)[[3, 7]].view(np.uint16), res.numpy()[[3, 7]].view(np.uint16))
+    with pytest.raises(wgs.WgsError, match="WGS_ERR_INDEX"):
+        wgs.check_error(DEV)
+
+
+def test_block_boundary_in_place():
+    st = synth.TINY_PADDED
+    dev = torch.device(DEV)
+    m = window_map(st).to(dev)
+    inv = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT).to(dev)
+    a, b = synth.residual_branch(st.tokens, 192, seed=16)
+    a, b = a.to(dev), b.to(dev)
+    r0, d0 = wgs.residual_add_norm_gather(a, b, m, EPS)
+    a2 = a.clone()
+    _, d1 = wgs.residual_add_norm_gather(a2, b, m, EPS, residual_out=a2)
+    assert torch.equal(a2.view(torch.int16), r0.view(torch.int16))
+    assert torch.equal(d1.view(torch.int16), d0.view(torch.int16))
+    windows = synth.gather_source(m.numel(), 192, seed=17).to(dev)
+    r0, y0 = wgs.window_reverse_add_ln_fwd(a, windows, inv, EPS)
+    a3 = a.clone()
+    _, y1 = wgs.window_reverse_add_ln_fwd(a3, windows, inv, EPS, residual_out=a3)
+    assert torch.equal(a3.view(torch.int16), r0.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y0.view(torch.int16))
+
+
 # ---------------------------------------------------------------- GELU ----
 
 def test_gelu_f32_full_size():
@@ -377,6 +479,7 @@ def test_identical_results_when_captured_in_a_cuda_graph():
     a, b, x, bias = synth.tiny_block(seed=3, stage=st)
     a, b, x, bias = a.to(dev), b.to(dev), x.to(dev), bias.to(dev)
     m = window_map(st).to(dev)
+    inv = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT).to(dev)
     xl = synth.ln_input(777, 384, seed=9).to(dev)
 
     def run(outs):
@@ -385,9 +488,15 @@ def test_identical_results_when_captured_in_a_cuda_graph():
         wgs.window_gather(a, m, out=outs["w"])
         wgs.ln_fwd(xl, EPS, out=outs["l"])
         wgs.bias_gelu_tanh(x, bias, out=outs["z"])
+        wgs.residual_add_norm_gather(a, b, m, EPS, residual_out=outs["r2"], out=outs["g2"])
+        wgs.window_reverse_add_ln_fwd(a, outs["w"], inv, EPS, residual_out=outs["r3"],
+                                      out=outs["y3"])
 
     def fresh():
-        return {"r": torch.empty_like(a), "y": torch.empty_like(a),
+        return {"r2": torch.empty_like(a), "g2": torch.empty(m.numel(), 192, dtype=torch.float16,
+                                                             device=dev),
+                "r3": torch.empty_like(a), "y3": torch.empty_like(a),
+                "r": torch.empty_like(a), "y": torch.empty_like(a),
                 "g": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
                 "w": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
                 "l": torch.empty_like(xl), "z": torch.empty_like(x)}

@@ -31,6 +31,9 @@ SIGNATURES = {
     "window_gather": (_st, [_P, _P, _P, _i64, _i64, _i32, _P]),
     "norm_gather": (_st, [_P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "bias_gelu_tanh": (_st, [_P, _P, _P, _i64, _i32, _i32, _P]),
+    "window_reverse_add_ln_fwd": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
+    "residual_add_norm_gather": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
+    "wgs_build_window_inverse": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
     "wgs_window_index_count": (_i64, [_P, _P, _P]),
     "wgs_build_window_index": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
     "wgs_check_error": (_st, [_P]),

@@ -131,6 +131,55 @@ def norm_gather(src: torch.Tensor, idx: torch.Tensor, eps: float = 1e-5,
     return dst
 
 
+# ------------------------------------------------ block-boundary fusions ----
+
+def window_reverse_add_ln_fwd(residual: torch.Tensor, windows: torch.Tensor,
+                              inv_idx: torch.Tensor, eps: float = 1e-5,
+                              residual_out: Optional[torch.Tensor] = None,
+                              out: Optional[torch.Tensor] = None):
+    """Returns (residual_out, y): residual_out[t] = fp16(residual[t] +
+    windows[inv_idx[t]]), y = LN(residual_out)."""
+    _cuda(residual, "residual", torch.float16)
+    _cuda(windows, "windows", torch.float16)
+    _cuda(inv_idx, "inv_idx", torch.int32)
+    _require(residual.dim() == 2 and windows.dim() == 2, "residual and windows must be 2-D")
+    rows, width = residual.shape
+    _require(windows.shape[1] == width, "windows must have the residual's width")
+    _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
+    _require(inv_idx.dim() == 1 and inv_idx.numel() == rows, "inv_idx must have one entry per row")
+    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
+    y = _out(out, residual.shape, torch.float16, residual.device, "out")
+    _same_device(residual, windows, inv_idx, r, y)
+    with torch.cuda.device(residual.device):
+        _capi.check("window_reverse_add_ln_fwd", _capi.load().window_reverse_add_ln_fwd(
+            _ptr(residual), _ptr(windows), _ptr(inv_idx), _ptr(r), _ptr(y), rows,
+            windows.shape[0], width, float(eps), _stream_ptr(residual.device)))
+    return r, y
+
+
+def residual_add_norm_gather(residual: torch.Tensor, branch: torch.Tensor, idx: torch.Tensor,
+                             eps: float = 1e-5, residual_out: Optional[torch.Tensor] = None,
+                             out: Optional[torch.Tensor] = None):
+    """Returns (residual_out, dst): residual_out = fp16(residual + branch),
+    dst[d] = LN(residual_out)[idx[d]] (zero row for -1)."""
+    _cuda(residual, "residual", torch.float16)
+    _cuda(branch, "branch", torch.float16)
+    _cuda(idx, "idx", torch.int32)
+    _require(residual.shape == branch.shape and residual.dim() == 2,
+             "residual and branch must be 2-D and of the same shape")
+    n_src, width = residual.shape
+    _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
+    _require(idx.dim() == 1, "idx must be 1-D")
+    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
+    dst = _out(out, (idx.numel(), width), torch.float16, residual.device, "out")
+    _same_device(residual, branch, idx, r, dst)
+    with torch.cuda.device(residual.device):
+        _capi.check("residual_add_norm_gather", _capi.load().residual_add_norm_gather(
+            _ptr(residual), _ptr(branch), _ptr(idx), _ptr(r), _ptr(dst), n_src, idx.numel(), width,
+            float(eps), _stream_ptr(residual.device)))
+    return r, dst
+
+
 # ---------------------------------------------------------------- GELU ----
 
 def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
@@ -178,6 +227,21 @@ def build_window_index(grid: Sequence[int], window: Sequence[int], shift: Sequen
     n = window_index_count(grid, window, padded)
     out = torch.empty(n, dtype=torch.int32)
     _capi.check("wgs_build_window_index", _capi.load().wgs_build_window_index(
+        _i3(grid, "grid"), _i3(window, "window"), _i3(shift, "shift"),
+        _i3(padded, "padded") if padded is not None else None, int(flags),
+        ctypes.c_void_p(out.data_ptr()), n))
+    return out if device is None else out.to(device)
+
+
+def build_window_inverse(grid: Sequence[int], window: Sequence[int], shift: Sequence[int],
+                         padded: Optional[Sequence[int]] = None, flags: int = SHIFT_THEN_PAD,
+                         device=None) -> torch.Tensor:
+    """inv[t] = the windowed row that holds token t (host-built); on `device` if given."""
+    n = 1
+    for g in grid:
+        n *= int(g)
+    out = torch.empty(n, dtype=torch.int32)
+    _capi.check("wgs_build_window_inverse", _capi.load().wgs_build_window_inverse(
         _i3(grid, "grid"), _i3(window, "window"), _i3(shift, "shift"),
         _i3(padded, "padded") if padded is not None else None, int(flags),
         ctypes.c_void_p(out.data_ptr()), n))

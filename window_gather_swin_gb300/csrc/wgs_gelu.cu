@@ -23,6 +23,8 @@
 // The op streams 2 x rows x width elements through HBM; the vector path
 // moves 16-byte chunks and keeps U independent chunks in flight per thread.
 // Bias chunks come through L1 (the whole bias row is at most a few KB).
+#include <atomic>
+
 #include "wgs_common.cuh"
 
 #ifndef WGS_GELU_THREADS
@@ -32,7 +34,12 @@
 #define WGS_GELU_U 4
 #endif
 #ifndef WGS_GELU_CTAS_PER_SM
-#define WGS_GELU_CTAS_PER_SM 8
+#define WGS_GELU_CTAS_PER_SM 0  // grid cap in CTAs per SM; 0: as many as can be resident
+#endif
+#ifdef WGS_GELU_MIN_CTAS  // optional register cap: resident CTAs per SM to aim for
+#define WGS_GELU_BOUNDS(T) __launch_bounds__(T, WGS_GELU_MIN_CTAS)
+#else
+#define WGS_GELU_BOUNDS(T) __launch_bounds__(T)
 #endif
 
 namespace wgs {
@@ -97,13 +104,13 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
             t[j] = __uint_as_float(word(xv, j)) + __uint_as_float(word(bv, j));
         }
     }
-    bool far = false;
+    float lowest = t[0];  // NaN elements need no redo: the fast form already gives NaN
 #pragma unroll
     for (int e = 0; e < kN; ++e) {
         y[e] = gelu_tanh_fast(t[e]);
-        far |= t[e] < kFarLeft;
+        lowest = fminf(lowest, t[e]);
     }
-    if (far) {
+    if (lowest < kFarLeft) {
 #pragma unroll
         for (int e = 0; e < kN; ++e)
             if (t[e] < kFarLeft) y[e] = gelu_tanh_far_left(t[e]);
@@ -123,7 +130,7 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
 // i mod row_vecs; each thread tracks that column incrementally (all steps
 // are below row_vecs, so one conditional subtraction keeps it in range).
 template <bool kHalf, int U, int THREADS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void WGS_GELU_BOUNDS(THREADS)
 bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec, int32_t row_vecs) {
     pdl_prologue();
     constexpr int64_t kTile = static_cast<int64_t>(THREADS) * U;
@@ -178,7 +185,7 @@ bias_gelu_scalar_kernel(const void *xp, const void *bp, void *yp, int64_t n, int
 
 template <bool kHalf>
 wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, int32_t width,
-                       int sm_count, cudaStream_t stream) {
+                       int device, int sm_count, cudaStream_t stream) {
     constexpr int kVec = kHalf ? 8 : 4;
     const int64_t n = rows * width;
     const bool vec = width % kVec == 0 && aligned16(x) && aligned16(bias) && aligned16(y);
@@ -186,8 +193,20 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
         constexpr int T = WGS_GELU_THREADS, U = WGS_GELU_U;
         const int64_t n_vec = n / kVec;
         const int64_t need = ceil_div(n_vec, static_cast<int64_t>(T) * U);
-        const int64_t cap = static_cast<int64_t>(sm_count) * WGS_GELU_CTAS_PER_SM;
-        return launch(bias_gelu_vec_kernel<kHalf, U, T>,
+        // One resident wave of grid-stride CTAs: a partial second wave
+        // would leave SMs idle at the end of this bandwidth-bound stream.
+        auto kernel = bias_gelu_vec_kernel<kHalf, U, T>;
+        static std::atomic<int> resident[64];  // per device, for this instantiation
+        int per_sm = WGS_GELU_CTAS_PER_SM > 0 ? WGS_GELU_CTAS_PER_SM
+                                              : resident[device].load(std::memory_order_relaxed);
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, T, 0) != cudaSuccess ||
+                per_sm < 1)
+                return WGS_ERR_LAUNCH;
+            resident[device].store(per_sm, std::memory_order_relaxed);
+        }
+        const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
+        return launch(kernel,
                       dim3(static_cast<unsigned>(need < cap ? need : cap)), dim3(T), 0, stream,
                       static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
                       static_cast<uint4 *>(y), n_vec, static_cast<int32_t>(width / kVec));
@@ -219,6 +238,7 @@ extern "C" wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, i
     DeviceInfo dev;
     const wgs_status st = current_device(&dev);
     if (st != WGS_OK) return st;
-    return dtype == WGS_F16 ? launch_gelu<true>(x, bias, y, rows, width, dev.sm_count, stream)
-                            : launch_gelu<false>(x, bias, y, rows, width, dev.sm_count, stream);
+    return dtype == WGS_F16
+               ? launch_gelu<true>(x, bias, y, rows, width, dev.device, dev.sm_count, stream)
+               : launch_gelu<false>(x, bias, y, rows, width, dev.device, dev.sm_count, stream);
 }

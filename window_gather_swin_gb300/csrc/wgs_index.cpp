@@ -84,3 +84,46 @@ extern "C" wgs_status wgs_build_window_index(const int32_t grid[3], const int32_
             }
     return WGS_OK;
 }
+
+// Inverse of the map above: inv[t] = the windowed row that holds token t.
+// Computed in closed form per token: the destination cell is the token's
+// coordinates rolled back by the shift (modulo the grid, or the padded grid
+// for pad-then-shift), and a cell's position in the window-major order is
+// the cells of all earlier window slabs / bands / windows plus its row-major
+// offset inside its own (possibly cut) window.
+extern "C" wgs_status wgs_build_window_inverse(const int32_t grid[3], const int32_t window[3],
+                                               const int32_t shift[3], const int32_t *padded,
+                                               int32_t flags, int32_t *inv_host, int64_t out_len) {
+    if (!grid || !window || !shift || !inv_host) return WGS_ERR_NULL;
+    if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
+    int64_t P[3];
+    if (!padded_extents(grid, window, padded, P)) return WGS_ERR_SHAPE;
+    const int64_t G[3] = {grid[0], grid[1], grid[2]};
+    if (P[0] * P[1] * P[2] > INT32_MAX) return WGS_ERR_SHAPE;
+    if (out_len < G[0] * G[1] * G[2]) return WGS_ERR_SHAPE;
+    const bool roll_padded = flags == WGS_PAD_THEN_SHIFT;
+    int64_t period[3], s[3], w[3];
+    for (int k = 0; k < 3; ++k) {
+        period[k] = roll_padded ? P[k] : G[k];
+        s[k] = wrap(shift[k], period[k]);
+        w[k] = window[k];
+    }
+    int64_t t = 0;
+    for (int64_t z = 0; z < G[0]; ++z)
+        for (int64_t h = 0; h < G[1]; ++h)
+            for (int64_t x = 0; x < G[2]; ++x) {
+                // destination cell c with c + shift = (z, h, x) modulo the period
+                const int64_t c[3] = {wrap(z - s[0], period[0]), wrap(h - s[1], period[1]),
+                                      wrap(x - s[2], period[2])};
+                int64_t b[3], e[3], i[3];
+                for (int k = 0; k < 3; ++k) {
+                    b[k] = c[k] / w[k];
+                    i[k] = c[k] % w[k];
+                    e[k] = P[k] - b[k] * w[k] < w[k] ? P[k] - b[k] * w[k] : w[k];
+                }
+                const int64_t start = b[0] * w[0] * P[1] * P[2] + e[0] * b[1] * w[1] * P[2] +
+                                      e[0] * e[1] * b[2] * w[2];
+                inv_host[t++] = static_cast<int32_t>(start + (i[0] * e[1] + i[1]) * e[2] + i[2]);
+            }
+    return WGS_OK;
+}

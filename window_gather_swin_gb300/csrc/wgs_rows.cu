@@ -33,16 +33,22 @@ namespace wgs {
 // [-1, n_src); read and cleared by wgs_check_error().
 __device__ unsigned int g_index_error;
 
-enum class RowOp : int { kLN, kAddLN, kGather, kNormGather };
+// kLN            y[r] = LN(x[r])
+// kAddLN         o[r] = fp16(a[r] + b[r]),         y[r] = LN(o[r])
+// kGather        y[r] = x[idx[r]]                  (zero row for a pad)
+// kNormGather    y[r] = LN(x[idx[r]])              (zero row for a pad)
+// kRevAddLN      o[r] = fp16(a[r] + w[inv[r]]),    y[r] = LN(o[r])
+// kAddNormGather o[s] = fp16(a[s] + b[s]),         y[r] = LN(o[s]),  s = idx[r]
+enum class RowOp : int { kLN, kAddLN, kGather, kNormGather, kRevAddLN, kAddNormGather };
 
 struct RowArgs {
-    const __half *in0;    // x (LN), residual (add + LN), src (gathers)
-    const __half *in1;    // branch (add + LN)
-    __half *out0;         // y (LN), residual_out (add + LN), dst (gathers)
-    __half *out1;         // y (add + LN)
-    const int32_t *idx;   // gathers
-    int64_t rows;         // rows (LN, add + LN) or n_idx (gathers)
-    int64_t n_src;        // gathers
+    const __half *in0;    // x / residual / src
+    const __half *in1;    // branch (add + LN, add + norm + gather), windows (reverse)
+    __half *out0;         // y (LN, gathers) or residual_out (the add ops)
+    __half *out1;         // y / dst of the add ops
+    const int32_t *idx;   // window map (gathers) or its inverse (reverse)
+    int64_t rows;         // rows of the launch: tokens, or windowed rows for the gathers
+    int64_t n_src;        // bound of idx values: source rows, or windowed rows (reverse)
     float eps;
 };
 
@@ -148,7 +154,11 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
     constexpr int CPL = WIDTH / 8 / LPR;
     constexpr int RPW = 32 / LPR;                 // rows per warp per group
     constexpr int ROWS_CTA = WARPS * RPW * U;     // rows per CTA per iteration
-    constexpr bool kGatherOp = OP == RowOp::kGather || OP == RowOp::kNormGather;
+    // index-driven rows: the launch's rows are windowed rows, read through idx
+    constexpr bool kByIndex =
+        OP == RowOp::kGather || OP == RowOp::kNormGather || OP == RowOp::kAddNormGather;
+    constexpr bool kTwoInputs =
+        OP == RowOp::kAddLN || OP == RowOp::kRevAddLN || OP == RowOp::kAddNormGather;
     constexpr bool kNorm = OP != RowOp::kGather;
     static_assert(LPR * CPL * 8 == WIDTH, "row tiling must cover the row");
 
@@ -161,22 +171,34 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
 
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * ROWS_CTA; base < a.rows;
          base += stride) {
-        int64_t row[U], src[U];
-        bool live[U], valid[U];
+        int64_t row[U], src[U], brow[U];
+        bool live[U], valid[U], branch[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             row[u] = base + static_cast<int64_t>(warp * U + u) * RPW + grp;
             live[u] = row[u] < a.rows;
             src[u] = row[u];
             valid[u] = live[u];
+            brow[u] = row[u];
+            branch[u] = live[u];
         }
-        if constexpr (kGatherOp) {
+        if constexpr (kByIndex || OP == RowOp::kRevAddLN) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int32_t s = live[u] ? __ldg(a.idx + row[u]) : -1;
-                valid[u] = s >= 0 && s < a.n_src;
-                if (live[u] && !valid[u] && s != -1 && sub == 0) atomicOr(&g_index_error, 1u);
-                src[u] = valid[u] ? s : 0;
+                const bool ok = s >= 0 && s < a.n_src;
+                // a pad (-1) is legal in a window map, never in its inverse
+                const bool legal = ok || (kByIndex && s == -1);
+                if (live[u] && !legal && sub == 0) atomicOr(&g_index_error, 1u);
+                if constexpr (kByIndex) {
+                    valid[u] = ok;
+                    src[u] = ok ? s : 0;
+                    brow[u] = src[u];
+                    branch[u] = ok;
+                } else {  // reverse: the residual row is always there, the branch row may not be
+                    branch[u] = live[u] && ok;
+                    brow[u] = ok ? s : 0;
+                }
             }
         }
 
@@ -187,30 +209,33 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
             for (int k = 0; k < CPL; ++k)
                 v[u][k] = valid[u] ? ld_stream(a.in0 + src[u] * WIDTH + (sub + k * LPR) * 8) : zero;
 
-        if constexpr (OP == RowOp::kAddLN) {
+        if constexpr (kTwoInputs) {
             uint4 b[U][CPL];
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int k = 0; k < CPL; ++k)
-                    b[u][k] = valid[u] ? ld_stream(a.in1 + row[u] * WIDTH + (sub + k * LPR) * 8)
-                                       : zero;
-            // residual_out = fp16(fp32 residual + fp32 branch)
+                    b[u][k] = branch[u] ? ld_stream(a.in1 + brow[u] * WIDTH + (sub + k * LPR) * 8)
+                                        : zero;
+            // residual_out = fp16(fp32 residual + fp32 branch); a missing
+            // branch (bad inverse index) leaves the residual bits unchanged
 #pragma unroll
             for (int u = 0; u < U; ++u)
+                if (branch[u])
 #pragma unroll
-                for (int k = 0; k < CPL; ++k) v[u][k] = add_fp16_chunk(v[u][k], b[u][k]);
+                    for (int k = 0; k < CPL; ++k) v[u][k] = add_fp16_chunk(v[u][k], b[u][k]);
+            // the residual stream is written at its own (source) row
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                if (live[u])
+                if (valid[u])
 #pragma unroll
                     for (int k = 0; k < CPL; ++k)
-                        st_stream(a.out0 + row[u] * WIDTH + (sub + k * LPR) * 8, v[u][k]);
+                        st_stream(a.out0 + src[u] * WIDTH + (sub + k * LPR) * 8, v[u][k]);
         }
 
         if constexpr (kNorm) ln_normalize<WIDTH, LPR, CPL, U>(v, a.eps);
 
-        __half *out = OP == RowOp::kAddLN ? a.out1 : a.out0;
+        __half *out = kTwoInputs ? a.out1 : a.out0;
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (live[u])
@@ -344,6 +369,56 @@ extern "C" wgs_status norm_gather(const void *src, const int32_t *idx, void *dst
     RowArgs a{static_cast<const __half *>(src), nullptr, static_cast<__half *>(dst), nullptr, idx,
               n_idx, n_src, eps};
     return dispatch_width<RowOp::kNormGather>(a, width, stream);
+}
+
+extern "C" wgs_status window_reverse_add_ln_fwd(const void *residual, const void *windows,
+                                                const int32_t *inv_idx, void *residual_out,
+                                                void *y, int64_t rows, int64_t n_windowed,
+                                                int32_t width, float eps, cudaStream_t stream) {
+    if (!ln_width(width)) return WGS_ERR_WIDTH;
+    if (rows < 0 || n_windowed < 0 || !fits(rows, width) || !fits(n_windowed, width))
+        return WGS_ERR_SHAPE;
+    if (rows == 0) return WGS_OK;
+    if (!residual || !inv_idx || !residual_out || !y || (n_windowed > 0 && !windows))
+        return WGS_ERR_NULL;
+    if (!aligned16(residual) || !aligned16(residual_out) || !aligned16(y) ||
+        (windows && !aligned16(windows)) || !aligned4(inv_idx))
+        return WGS_ERR_ALIGN;
+    const int64_t bytes = rows * width * 2;
+    const int64_t wbytes = n_windowed * width * 2;
+    if (overlap(residual_out, bytes, y, bytes) || !same_or_disjoint(residual_out, residual, bytes) ||
+        !same_or_disjoint(y, residual, bytes) || overlap(windows, wbytes, residual_out, bytes) ||
+        overlap(windows, wbytes, y, bytes) || overlap(inv_idx, rows * 4, residual_out, bytes) ||
+        overlap(inv_idx, rows * 4, y, bytes))
+        return WGS_ERR_ALIAS;
+    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(windows),
+              static_cast<__half *>(residual_out), static_cast<__half *>(y), inv_idx, rows,
+              n_windowed, eps};
+    return dispatch_width<RowOp::kRevAddLN>(a, width, stream);
+}
+
+extern "C" wgs_status residual_add_norm_gather(const void *residual, const void *branch,
+                                               const int32_t *idx, void *residual_out, void *dst,
+                                               int64_t n_src, int64_t n_idx, int32_t width,
+                                               float eps, cudaStream_t stream) {
+    if (!ln_width(width)) return WGS_ERR_WIDTH;
+    if (n_src < 0 || n_idx < 0 || !fits(n_src, width) || !fits(n_idx, width)) return WGS_ERR_SHAPE;
+    if (n_idx == 0) return WGS_OK;
+    if (!idx || !dst || (n_src > 0 && (!residual || !branch || !residual_out))) return WGS_ERR_NULL;
+    if (!aligned16(dst) || !aligned4(idx) ||
+        (n_src > 0 && (!aligned16(residual) || !aligned16(branch) || !aligned16(residual_out))))
+        return WGS_ERR_ALIGN;
+    const int64_t bytes = n_src * width * 2;
+    const int64_t dbytes = n_idx * width * 2;
+    if (!same_or_disjoint(residual_out, residual, bytes) ||
+        !same_or_disjoint(residual_out, branch, bytes) || overlap(dst, dbytes, residual, bytes) ||
+        overlap(dst, dbytes, branch, bytes) || overlap(dst, dbytes, residual_out, bytes) ||
+        overlap(idx, n_idx * 4, dst, dbytes) || overlap(idx, n_idx * 4, residual_out, bytes))
+        return WGS_ERR_ALIAS;
+    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(branch),
+              static_cast<__half *>(residual_out), static_cast<__half *>(dst), idx, n_idx, n_src,
+              eps};
+    return dispatch_width<RowOp::kAddNormGather>(a, width, stream);
 }
 
 extern "C" wgs_status wgs_check_error(cudaStream_t stream) {
