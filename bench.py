@@ -368,7 +368,7 @@ def run_ours(args, rank, world, local):
     init_dist(world, "nccl")
     calls = build_calls()
     if args.only:
-        calls = [c for c in calls if args.only in c.label]
+        calls = [c for c in calls + build_next_calls() if args.only in c.label]
         if not calls:
             raise SystemExit(f"--only {args.only!r} matches no call")
     props = torch.cuda.get_device_properties(dev)
