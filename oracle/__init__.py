@@ -8,7 +8,8 @@ benchmark's CPU-baseline leg import this package; the library in
 The arithmetic lives in ``wgs_oracle.c`` (plain C, double precision, one
 element at a time).  This module only marshals numpy arrays through ctypes.
 fp16 tensors are passed as ``numpy.float16`` arrays and handled as their
-binary16 bit patterns.
+binary16 bit patterns.  bfloat16 tensors (``fmt="bf16"``) travel as
+``numpy.uint16`` arrays of their bit patterns, numpy having no bfloat16 type.
 """
 import ctypes
 import os
@@ -32,6 +33,16 @@ def _load():
             "orc_rn16": (ctypes.c_uint16, [ctypes.c_double]),
             "orc_rn16_array": (None, [P, P, i64]),
             "orc_f16_to_f64_array": (None, [P, P, i64]),
+            "orc_rnbf16_array": (None, [P, P, i64]),
+            "orc_bf16_to_f64_array": (None, [P, P, i64]),
+            "orc_ln_fmt": (None, [P, P, i64, i32, f32, ctypes.c_int]),
+            "orc_ln_f64_fmt": (None, [P, P, i64, i32, f32, ctypes.c_int]),
+            "orc_residual_add_ln_fmt": (None, [P, P, P, P, i64, i32, f32, ctypes.c_int]),
+            "orc_norm_gather_fmt": (i64, [P, P, P, i64, i64, i32, f32, ctypes.c_int]),
+            "orc_bias_gelu_16": (None, [P, P, P, P, i64, i32, ctypes.c_int]),
+            "orc_window_reverse_add_ln_fmt": (i64, [P, P, P, P, P, i64, i64, i32, f32, ctypes.c_int]),
+            "orc_residual_add_norm_gather_fmt": (i64, [P, P, P, P, P, i64, i64, i32, f32,
+                                                       ctypes.c_int]),
             "orc_ln_row_f64": (None, [P, P, i32, f32]),
             "orc_ln": (None, [P, P, i64, i32, f32]),
             "orc_ln_f64": (None, [P, P, i64, i32, f32]),
@@ -85,6 +96,31 @@ def f16_to_f64(values) -> np.ndarray:
     return out
 
 
+def rnbf16(values) -> np.ndarray:
+    """Round doubles to bfloat16 (nearest, ties to even); returns uint16 bits."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().orc_rnbf16_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact double value of each bfloat16 bit pattern."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().orc_bf16_to_f64_array(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+_FMT = {"f16": (0, np.float16), "bf16": (1, np.uint16)}
+
+
+def _fmt(fmt):
+    if fmt not in _FMT:
+        raise ValueError("fmt must be 'f16' or 'bf16'")
+    return _FMT[fmt]
+
+
 # ------------------------------------------------------------------ LN ----
 
 def ln_row_f64(x, eps: float = 1e-5) -> np.ndarray:
@@ -95,32 +131,36 @@ def ln_row_f64(x, eps: float = 1e-5) -> np.ndarray:
     return y
 
 
-def ln(x, eps: float = 1e-5) -> np.ndarray:
-    """No-affine LayerNorm of fp16 rows [rows, width] -> fp16."""
-    x = _c(x, np.float16)
+def ln(x, eps: float = 1e-5, fmt: str = "f16") -> np.ndarray:
+    """No-affine LayerNorm of 16-bit rows [rows, width] -> same format."""
+    code, dt = _fmt(fmt)
+    x = _c(x, dt)
     rows, width = x.shape
     y = np.empty_like(x)
-    _load().orc_ln(_ptr(x), _ptr(y), rows, width, eps)
+    _load().orc_ln_fmt(_ptr(x), _ptr(y), rows, width, eps, code)
     return y
 
 
-def ln_f64(x, eps: float = 1e-5) -> np.ndarray:
-    """Unrounded (double) LN outputs of fp16 rows."""
-    x = _c(x, np.float16)
+def ln_f64(x, eps: float = 1e-5, fmt: str = "f16") -> np.ndarray:
+    """Unrounded (double) LN outputs of 16-bit rows."""
+    code, dt = _fmt(fmt)
+    x = _c(x, dt)
     rows, width = x.shape
     y = np.empty(x.shape, dtype=np.float64)
-    _load().orc_ln_f64(_ptr(x), _ptr(y), rows, width, eps)
+    _load().orc_ln_f64_fmt(_ptr(x), _ptr(y), rows, width, eps, code)
     return y
 
 
-def residual_add_ln(residual, branch, eps: float = 1e-5):
-    """Returns (residual_out, y), both fp16."""
-    a = _c(residual, np.float16)
-    b = _c(branch, np.float16)
+def residual_add_ln(residual, branch, eps: float = 1e-5, fmt: str = "f16"):
+    """Returns (residual_out, y), both in the input format."""
+    code, dt = _fmt(fmt)
+    a = _c(residual, dt)
+    b = _c(branch, dt)
     assert a.shape == b.shape and a.ndim == 2
     r = np.empty_like(a)
     y = np.empty_like(a)
-    _load().orc_residual_add_ln(_ptr(a), _ptr(b), _ptr(r), _ptr(y), a.shape[0], a.shape[1], eps)
+    _load().orc_residual_add_ln_fmt(_ptr(a), _ptr(b), _ptr(r), _ptr(y), a.shape[0], a.shape[1],
+                                    eps, code)
     return r, y
 
 
@@ -155,28 +195,31 @@ def window_gather(src, idx):
     return dst, int(bad)
 
 
-def norm_gather(src, idx, eps: float = 1e-5):
+def norm_gather(src, idx, eps: float = 1e-5, fmt: str = "f16"):
     """Returns (dst, number of indices outside [-1, n_src))."""
-    s = _c(src, np.float16)
+    code, dt = _fmt(fmt)
+    s = _c(src, dt)
     i = _c(idx, np.int32).ravel()
-    dst = np.empty((i.size, s.shape[1]), dtype=np.float16)
-    bad = _load().orc_norm_gather(_ptr(s), _ptr(i), _ptr(dst), s.shape[0], i.size, s.shape[1], eps)
+    dst = np.empty((i.size, s.shape[1]), dtype=dt)
+    bad = _load().orc_norm_gather_fmt(_ptr(s), _ptr(i), _ptr(dst), s.shape[0], i.size, s.shape[1],
+                                      eps, code)
     return dst, int(bad)
 
 
 # ------------------------------------------------ block-boundary fusions ----
 
-def window_reverse_add_ln(residual, attn, idx, eps: float = 1e-5):
-    """Returns (residual_out, y, anomalies): r[t] = fp16(residual[t] + attn[d])
+def window_reverse_add_ln(residual, attn, idx, eps: float = 1e-5, fmt: str = "f16"):
+    """Returns (residual_out, y, anomalies): r[t] = round(residual[t] + attn[d])
     for the windowed row d with idx[d] == t, y = LN(r)."""
-    r = _c(residual, np.float16)
-    w = _c(attn, np.float16)
+    code, dt = _fmt(fmt)
+    r = _c(residual, dt)
+    w = _c(attn, dt)
     i = _c(idx, np.int32).ravel()
     assert r.ndim == 2 and w.ndim == 2 and r.shape[1] == w.shape[1] and w.shape[0] == i.size
     r_out = np.empty_like(r)
     y = np.empty_like(r)
-    bad = _load().orc_window_reverse_add_ln(_ptr(r), _ptr(w), _ptr(i), _ptr(r_out), _ptr(y),
-                                            r.shape[0], i.size, r.shape[1], eps)
+    bad = _load().orc_window_reverse_add_ln_fmt(_ptr(r), _ptr(w), _ptr(i), _ptr(r_out), _ptr(y),
+                                                r.shape[0], i.size, r.shape[1], eps, code)
     return r_out, y, int(bad)
 
 
@@ -188,38 +231,44 @@ def invert_window_index(idx, n_tokens: int) -> np.ndarray:
     return inv
 
 
-def residual_add_norm_gather(residual, branch, idx, eps: float = 1e-5):
-    """Returns (residual_out, dst, bad): r = fp16(residual + branch),
+def residual_add_norm_gather(residual, branch, idx, eps: float = 1e-5, fmt: str = "f16"):
+    """Returns (residual_out, dst, bad): r = round(residual + branch),
     dst[d] = LN(r)[idx[d]] (zero row for -1)."""
-    a = _c(residual, np.float16)
-    b = _c(branch, np.float16)
+    code, dt = _fmt(fmt)
+    a = _c(residual, dt)
+    b = _c(branch, dt)
     i = _c(idx, np.int32).ravel()
     assert a.shape == b.shape and a.ndim == 2
     r = np.empty_like(a)
-    dst = np.empty((i.size, a.shape[1]), dtype=np.float16)
-    bad = _load().orc_residual_add_norm_gather(_ptr(a), _ptr(b), _ptr(i), _ptr(r), _ptr(dst),
-                                               a.shape[0], i.size, a.shape[1], eps)
+    dst = np.empty((i.size, a.shape[1]), dtype=dt)
+    bad = _load().orc_residual_add_norm_gather_fmt(_ptr(a), _ptr(b), _ptr(i), _ptr(r), _ptr(dst),
+                                                   a.shape[0], i.size, a.shape[1], eps, code)
     return r, dst, int(bad)
 
 
 # ---------------------------------------------------------------- GELU ----
 
-def bias_gelu_tanh(x, bias, want_f64: bool = True):
-    """Returns (y, y64): y in the dtype of x (float32 or float16), y64 the
-    unrounded double result (None unless want_f64)."""
+def bias_gelu_tanh(x, bias, want_f64: bool = True, fmt: str = None):
+    """Returns (y, y64): y in the format of x (float32, float16, or bfloat16
+    bits with fmt="bf16"), y64 the unrounded double result (None unless
+    want_f64)."""
     x = np.asarray(x)
     lib = _load()
-    if x.dtype == np.float32:
+    rows, width = x.shape
+    y64 = np.empty(x.shape, dtype=np.float64) if want_f64 else None
+    if fmt is None and x.dtype == np.float32:
         xs, bs = _c(x, np.float32), _c(bias, np.float32)
-        fn = lib.orc_bias_gelu_f32
-    elif x.dtype == np.float16:
-        xs, bs = _c(x, np.float16), _c(bias, np.float16)
-        fn = lib.orc_bias_gelu_f16
-    else:
-        raise TypeError("bias_gelu_tanh oracle takes float32 or float16")
-    rows, width = xs.shape
+        assert bs.shape == (width,)
+        y = np.empty_like(xs)
+        lib.orc_bias_gelu_f32(_ptr(xs), _ptr(bs), _ptr(y), _ptr(y64), rows, width)
+        return y, y64
+    if fmt is None and x.dtype == np.float16:
+        fmt = "f16"
+    if fmt is None:
+        raise TypeError("bias_gelu_tanh oracle takes float32, float16 or fmt='bf16' bits")
+    code, dt = _fmt(fmt)
+    xs, bs = _c(x, dt), _c(bias, dt)
     assert bs.shape == (width,)
     y = np.empty_like(xs)
-    y64 = np.empty(xs.shape, dtype=np.float64) if want_f64 else None
-    fn(_ptr(xs), _ptr(bs), _ptr(y), _ptr(y64), rows, width)
+    lib.orc_bias_gelu_16(_ptr(xs), _ptr(bs), _ptr(y), _ptr(y64), rows, width, code)
     return y, y64

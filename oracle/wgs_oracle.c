@@ -72,7 +72,7 @@ uint16_t orc_rn16(double v)
         return (uint16_t)(sign | (uint16_t)n); /* n == 1024 encodes 2^-14 */
     }
     int ex;
-    double m = frexp(a, &ex);       /* a = m * 2^ex, m in [0.5, 1) */
+    frexp(a, &ex);                 /* a = m * 2^ex, m in [0.5, 1) */
     int E = ex - 1;                 /* a = (2m) * 2^E, 2m in [1, 2) */
     double n = round_half_even(ldexp(a, 10 - E)); /* in [1024, 2048] */
     if (n == 2048.0) { n = 1024.0; E += 1; }
@@ -90,6 +90,60 @@ void orc_f16_to_f64_array(const uint16_t *h, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_f64(h[i]);
 }
+
+/* bfloat16: the top half of a binary32 (8 exponent bits, 7 fraction bits). */
+double orc_bf16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int m = h & 0x7F;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -133);            /* subnormal or zero */
+    } else if (e == 255) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + m), e - 134); /* (1 + m/128) * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+/* double -> bfloat16 bits, round to nearest, ties to even, as orc_rn16 but
+ * with 7 fraction bits and binary32's exponent range. */
+uint16_t orc_rnbf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return (uint16_t)(sign | 0x7FC0);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    /* largest finite (2 - 2^-7) 2^127; the midpoint to 2^128 ties to inf */
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127)) return (uint16_t)(sign | 0x7F80);
+    if (a < ldexp(1.0, -126)) {
+        double n = round_half_even(ldexp(a, 133)); /* quantum 2^-133 */
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    int ex;
+    frexp(a, &ex);
+    int E = ex - 1;
+    double n = round_half_even(ldexp(a, 7 - E)); /* in [128, 256] */
+    if (n == 256.0) { n = 128.0; E += 1; }
+    if (E + 127 >= 255) return (uint16_t)(sign | 0x7F80);
+    return (uint16_t)(sign | (uint16_t)((E + 127) << 7) | (uint16_t)(n - 128.0));
+}
+
+void orc_rnbf16_array(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_rnbf16(v[i]);
+}
+
+void orc_bf16_to_f64_array(const uint16_t *h, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_to_f64(h[i]);
+}
+
+/* The 16-bit storage formats of the row ops: fmt 0 = binary16, 1 = bfloat16. */
+static double dec16(uint16_t h, int fmt) { return fmt ? orc_bf16_to_f64(h) : orc_f16_to_f64(h); }
+static uint16_t enc16(double v, int fmt) { return fmt ? orc_rnbf16(v) : orc_rn16(v); }
 
 /* ------------------------------------------------------------------ */
 /* LayerNorm without affine  [P1 s3]                                   */
@@ -113,31 +167,41 @@ void orc_ln_row_f64(const double *x, double *y, int32_t width, float eps)
     for (int32_t i = 0; i < width; ++i) y[i] = (x[i] - mean) / denom;
 }
 
-/* fp16 rows in, fp16 rows out: each output is the rounding of the exact
- * (double) normalised value. */
-void orc_ln(const uint16_t *x, uint16_t *y, int64_t rows, int32_t width, float eps)
+/* 16-bit rows in, 16-bit rows out (format fmt): each output is the rounding
+ * of the exact (double) normalised value. */
+void orc_ln_fmt(const uint16_t *x, uint16_t *y, int64_t rows, int32_t width, float eps, int fmt)
 {
     double *xd = (double *)malloc(sizeof(double) * (size_t)width);
     double *yd = (double *)malloc(sizeof(double) * (size_t)width);
     for (int64_t r = 0; r < rows; ++r) {
         const uint16_t *xr = x + r * (int64_t)width;
-        for (int32_t i = 0; i < width; ++i) xd[i] = orc_f16_to_f64(xr[i]);
+        for (int32_t i = 0; i < width; ++i) xd[i] = dec16(xr[i], fmt);
         orc_ln_row_f64(xd, yd, width, eps);
-        for (int32_t i = 0; i < width; ++i) y[r * (int64_t)width + i] = orc_rn16(yd[i]);
+        for (int32_t i = 0; i < width; ++i) y[r * (int64_t)width + i] = enc16(yd[i], fmt);
     }
     free(xd);
     free(yd);
 }
 
-/* Unrounded LN outputs of fp16 rows, for tolerance decisions. */
-void orc_ln_f64(const uint16_t *x, double *y, int64_t rows, int32_t width, float eps)
+void orc_ln(const uint16_t *x, uint16_t *y, int64_t rows, int32_t width, float eps)
+{
+    orc_ln_fmt(x, y, rows, width, eps, 0);
+}
+
+/* Unrounded LN outputs of 16-bit rows, for tolerance decisions. */
+void orc_ln_f64_fmt(const uint16_t *x, double *y, int64_t rows, int32_t width, float eps, int fmt)
 {
     double *xd = (double *)malloc(sizeof(double) * (size_t)width);
     for (int64_t r = 0; r < rows; ++r) {
-        for (int32_t i = 0; i < width; ++i) xd[i] = orc_f16_to_f64(x[r * (int64_t)width + i]);
+        for (int32_t i = 0; i < width; ++i) xd[i] = dec16(x[r * (int64_t)width + i], fmt);
         orc_ln_row_f64(xd, y + r * (int64_t)width, width, eps);
     }
     free(xd);
+}
+
+void orc_ln_f64(const uint16_t *x, double *y, int64_t rows, int32_t width, float eps)
+{
+    orc_ln_f64_fmt(x, y, rows, width, eps, 0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -150,13 +214,21 @@ void orc_ln_f64(const uint16_t *x, double *y, int64_t rows, int32_t width, float
  * carries 24 >= 2*11 + 2 significand bits, rounding first to binary32 and
  * then to binary16 gives the same result as rounding the exact sum once
  * (Figueroa, "When is double rounding innocuous?", 1995). */
+void orc_residual_add_ln_fmt(const uint16_t *a, const uint16_t *b, uint16_t *r_out, uint16_t *y,
+                             int64_t rows, int32_t width, float eps, int fmt)
+{
+    int64_t n = rows * (int64_t)width;
+    for (int64_t i = 0; i < n; ++i) r_out[i] = enc16(dec16(a[i], fmt) + dec16(b[i], fmt), fmt);
+    orc_ln_fmt(r_out, y, rows, width, eps, fmt);
+}
+
+/* bfloat16 (fmt 1) keeps the same rounding point: binary32's 24 bits are
+ * at least 2 * 8 + 2, so fp32 then bfloat16 equals one rounding of the
+ * exact sum. */
 void orc_residual_add_ln(const uint16_t *a, const uint16_t *b, uint16_t *r_out, uint16_t *y,
                          int64_t rows, int32_t width, float eps)
 {
-    int64_t n = rows * (int64_t)width;
-    for (int64_t i = 0; i < n; ++i)
-        r_out[i] = orc_rn16(orc_f16_to_f64(a[i]) + orc_f16_to_f64(b[i]));
-    orc_ln(r_out, y, rows, width, eps);
+    orc_residual_add_ln_fmt(a, b, r_out, y, rows, width, eps, 0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -283,21 +355,27 @@ int64_t orc_window_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst
 /* dst[d] = LN(src[idx[d]]) for idx[d] >= 0, zero row for -1: the
  * normalised tensor is defined row by row, so this is LN applied to each
  * gathered row. */
-int64_t orc_norm_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst,
-                        int64_t n_src, int64_t n_idx, int32_t width, float eps)
+int64_t orc_norm_gather_fmt(const uint16_t *src, const int32_t *idx, uint16_t *dst,
+                            int64_t n_src, int64_t n_idx, int32_t width, float eps, int fmt)
 {
     int64_t bad = 0;
     for (int64_t d = 0; d < n_idx; ++d) {
         int64_t s = idx[d];
         uint16_t *out = dst + d * (int64_t)width;
         if (s >= 0 && s < n_src) {
-            orc_ln(src + s * (int64_t)width, out, 1, width, eps);
+            orc_ln_fmt(src + s * (int64_t)width, out, 1, width, eps, fmt);
         } else {
             if (s != -1) ++bad;
             for (int32_t i = 0; i < width; ++i) out[i] = 0;
         }
     }
     return bad;
+}
+
+int64_t orc_norm_gather(const uint16_t *src, const int32_t *idx, uint16_t *dst,
+                        int64_t n_src, int64_t n_idx, int32_t width, float eps)
+{
+    return orc_norm_gather_fmt(src, idx, dst, n_src, n_idx, width, eps, 0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -338,19 +416,26 @@ void orc_bias_gelu_f32(const float *x, const float *bias, float *y, double *y64,
         }
 }
 
-/* fp16: t = fp16(x + bias[col]), keeping the rounding point an eager
- * `gelu(x + bias)` in half precision would have; y = fp16(gelu(t)). */
-void orc_bias_gelu_f16(const uint16_t *x, const uint16_t *bias, uint16_t *y, double *y64,
-                       int64_t rows, int32_t width)
+/* 16-bit formats: t = fp16(x + bias[col]) (or bfloat16), keeping the
+ * rounding point an eager `gelu(x + bias)` in that precision would have;
+ * y = round(gelu(t)). */
+void orc_bias_gelu_16(const uint16_t *x, const uint16_t *bias, uint16_t *y, double *y64,
+                      int64_t rows, int32_t width, int fmt)
 {
     for (int64_t r = 0; r < rows; ++r)
         for (int32_t c = 0; c < width; ++c) {
             int64_t i = r * (int64_t)width + c;
-            uint16_t t = orc_rn16(orc_f16_to_f64(x[i]) + orc_f16_to_f64(bias[c]));
-            double g = gelu_tanh(orc_f16_to_f64(t));
+            uint16_t t = enc16(dec16(x[i], fmt) + dec16(bias[c], fmt), fmt);
+            double g = gelu_tanh(dec16(t, fmt));
             if (y64) y64[i] = g;
-            if (y) y[i] = orc_rn16(g);
+            if (y) y[i] = enc16(g, fmt);
         }
+}
+
+void orc_bias_gelu_f16(const uint16_t *x, const uint16_t *bias, uint16_t *y, double *y64,
+                       int64_t rows, int32_t width)
+{
+    orc_bias_gelu_16(x, bias, y, y64, rows, width, 0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -368,9 +453,10 @@ void orc_bias_gelu_f16(const uint16_t *x, const uint16_t *bias, uint16_t *y, dou
  * that no windowed row names takes a zero branch (r = residual) and is
  * counted, as is a token named more than once (the last row wins).
  * Returns that count (0 for any map from orc_build_window_index). */
-int64_t orc_window_reverse_add_ln(const uint16_t *residual, const uint16_t *attn,
-                                  const int32_t *idx, uint16_t *r_out, uint16_t *y,
-                                  int64_t n_tokens, int64_t n_idx, int32_t width, float eps)
+int64_t orc_window_reverse_add_ln_fmt(const uint16_t *residual, const uint16_t *attn,
+                                      const int32_t *idx, uint16_t *r_out, uint16_t *y,
+                                      int64_t n_tokens, int64_t n_idx, int32_t width, float eps,
+                                      int fmt)
 {
     int32_t *seen = (int32_t *)calloc((size_t)(n_tokens > 0 ? n_tokens : 1), sizeof(int32_t));
     for (int64_t t = 0; t < n_tokens * (int64_t)width; ++t) r_out[t] = residual[t];
@@ -380,14 +466,22 @@ int64_t orc_window_reverse_add_ln(const uint16_t *residual, const uint16_t *attn
         seen[t] += 1;
         for (int32_t i = 0; i < width; ++i) {
             int64_t k = t * (int64_t)width + i;
-            r_out[k] = orc_rn16(orc_f16_to_f64(residual[k]) + orc_f16_to_f64(attn[d * (int64_t)width + i]));
+            r_out[k] = enc16(dec16(residual[k], fmt) + dec16(attn[d * (int64_t)width + i], fmt), fmt);
         }
     }
     int64_t bad = 0;
     for (int64_t t = 0; t < n_tokens; ++t) bad += seen[t] != 1;
     free(seen);
-    orc_ln(r_out, y, n_tokens, width, eps);
+    orc_ln_fmt(r_out, y, n_tokens, width, eps, fmt);
     return bad;
+}
+
+int64_t orc_window_reverse_add_ln(const uint16_t *residual, const uint16_t *attn,
+                                  const int32_t *idx, uint16_t *r_out, uint16_t *y,
+                                  int64_t n_tokens, int64_t n_idx, int32_t width, float eps)
+{
+    return orc_window_reverse_add_ln_fmt(residual, attn, idx, r_out, y, n_tokens, n_idx, width,
+                                         eps, 0);
 }
 
 /* token -> windowed row: inv[idx[d]] = d; tokens no row names get -1 */
@@ -407,13 +501,20 @@ void orc_invert_window_index(const int32_t *idx, int64_t n_idx, int32_t *inv, in
  *     r = fp16(a + b),   dst[d] = LN(r)[idx[d]]  (zero row for -1).
  * Written as the composition of the two definitions above.  Returns the
  * number of indices outside [-1, n_src). */
+int64_t orc_residual_add_norm_gather_fmt(const uint16_t *a, const uint16_t *b, const int32_t *idx,
+                                         uint16_t *r_out, uint16_t *dst, int64_t n_src,
+                                         int64_t n_idx, int32_t width, float eps, int fmt)
+{
+    uint16_t *y = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(n_src * (int64_t)width + 1));
+    orc_residual_add_ln_fmt(a, b, r_out, y, n_src, width, eps, fmt);
+    int64_t bad = orc_window_gather(y, idx, dst, n_src, n_idx, width);
+    free(y);
+    return bad;
+}
+
 int64_t orc_residual_add_norm_gather(const uint16_t *a, const uint16_t *b, const int32_t *idx,
                                      uint16_t *r_out, uint16_t *dst, int64_t n_src,
                                      int64_t n_idx, int32_t width, float eps)
 {
-    uint16_t *y = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(n_src * (int64_t)width + 1));
-    orc_residual_add_ln(a, b, r_out, y, n_src, width, eps);
-    int64_t bad = orc_window_gather(y, idx, dst, n_src, n_idx, width);
-    free(y);
-    return bad;
+    return orc_residual_add_norm_gather_fmt(a, b, idx, r_out, dst, n_src, n_idx, width, eps, 0);
 }

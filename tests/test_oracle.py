@@ -474,3 +474,75 @@ def test_residual_add_norm_gather_matches_numpy_composition():
     ln = oracle.ln(want_r, EPS)
     want = np.where((m >= 0)[:, None], ln[np.maximum(m, 0)], np.float16(0))
     assert np.array_equal(dst.view(np.uint16), want.view(np.uint16))
+
+
+# ------------------------------------------------------------ bfloat16 ----
+
+def _all_bf16_bits():
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+def _torch_bf16_of_bits(bits):
+    return torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16)
+
+
+def _bits_of_torch_bf16(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_decode_matches_torch_on_every_pattern():
+    bits = _all_bf16_bits()
+    ours = oracle.bf16_to_f64(bits)
+    ref = _torch_bf16_of_bits(bits).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_rnbf16_round_trips_and_matches_torch():
+    bits = _all_bf16_bits()
+    vals = oracle.bf16_to_f64(bits)
+    ok = ~np.isnan(vals)
+    assert np.array_equal(oracle.rnbf16(vals[ok]), bits[ok])
+    rng = np.random.default_rng(17)
+    f = (np.exp2(rng.uniform(-140, 127, 300_000)) * rng.choice([-1, 1], 300_000)).astype(np.float32)
+    want = _bits_of_torch_bf16(torch.from_numpy(f).to(torch.bfloat16))
+    assert np.array_equal(oracle.rnbf16(f.astype(np.float64)), want)
+
+
+def test_rnbf16_ties_go_to_even_and_range_edges():
+    pos = oracle.bf16_to_f64(np.arange(0x7F80, dtype=np.uint16))  # +0 .. largest finite
+    lo, hi = pos[:-1], pos[1:]
+    mid = (lo + hi) / 2.0
+    lo_b, hi_b = oracle.rnbf16(lo), oracle.rnbf16(hi)
+    assert np.array_equal(oracle.rnbf16(mid), np.where(lo_b % 2 == 0, lo_b, hi_b))
+    bits = lambda v: int(oracle.rnbf16(np.array([v]))[0])
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    assert bits(big) == 0x7F7F
+    assert bits((2.0 - 2.0 ** -8) * 2.0 ** 127) == 0x7F80   # tie above the largest finite
+    assert bits(2.0 ** -133) == 0x0001
+    assert bits(2.0 ** -134) == 0x0000                      # tie between 0 and 2^-133
+
+
+def test_bf16_residual_add_ln():
+    g = torch.Generator().manual_seed(3)
+    a = torch.randn(96, 192, generator=g).to(torch.bfloat16)
+    b = (torch.randn(96, 192, generator=g) * 0.1).to(torch.bfloat16)
+    r, y = oracle.residual_add_ln(_bits_of_torch_bf16(a), _bits_of_torch_bf16(b), EPS, fmt="bf16")
+    assert np.array_equal(r, _bits_of_torch_bf16(a + b))     # torch: fp32 add, round to bf16
+    r64 = _torch_bf16_of_bits(r).double()
+    ref = torch.nn.functional.layer_norm(r64, (192,), eps=EPS).numpy()
+    assert np.max(np.abs(oracle.ln_f64(r, EPS, fmt="bf16") - ref)) < 1e-12
+    assert np.array_equal(y, oracle.rnbf16(ref))
+
+
+def test_bf16_gelu():
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(32, 768, generator=g).to(torch.bfloat16)
+    b = (torch.randn(768, generator=g) * 0.02).to(torch.bfloat16)
+    y, y64 = oracle.bias_gelu_tanh(_bits_of_torch_bf16(x), _bits_of_torch_bf16(b), fmt="bf16")
+    t = (x + b[None, :]).double()
+    ref = torch.nn.functional.gelu(t, approximate="tanh").numpy()
+    assert _close_to_torch(y64, t.numpy(), ref)
+    assert np.array_equal(y, oracle.rnbf16(ref))
