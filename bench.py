@@ -148,6 +148,28 @@ def build_next_calls():
             lambda i, o: wgs.residual_add_norm_gather(i["a"], i["b"], i["idx"], EPS,
                                                       residual_out=o["r"], out=o["dst"]),
             None, m))
+    # bfloat16 forms at the large stage / MLP width
+    st = synth.STAGE_192
+    n, c = st.tokens, st.width
+    bf = torch.bfloat16
+    xb = synth.ln_input(n, c, seed=1, dtype=bf)
+    calls.append(Call("ln_fwd", f"bf16 [{n},{c}]", 4 * n * c, {"x": xb},
+                      {"y": ((n, c), bf)}, lambda i, o: wgs.ln_fwd(i["x"], EPS, out=o["y"]),
+                      None, n))
+    idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+    m = idx.numel()
+    ab, bb = synth.residual_branch(n, c, seed=2, dtype=bf)
+    calls.append(Call(
+        "residual_add_norm_gather", f"bf16 [{n},{c}]->{m}", 6 * n * c + (2 * c + 4) * m,
+        {"a": ab, "b": bb, "idx": idx}, {"r": ((n, c), bf), "dst": ((m, c), bf)},
+        lambda i, o: wgs.residual_add_norm_gather(i["a"], i["b"], i["idx"], EPS,
+                                                  residual_out=o["r"], out=o["dst"]),
+        None, m))
+    rows, width = synth.GELU_F16_SHAPE
+    xg, bg = synth.gelu_input(rows, width, bf, seed=4)
+    calls.append(Call("bias_gelu_tanh", f"bf16 [{rows},{width}]", 4 * rows * width + 2 * width,
+                      {"x": xg, "bias": bg}, {"y": ((rows, width), bf)},
+                      lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]), None, rows))
     return calls
 
 
@@ -210,11 +232,11 @@ KERNEL_SOURCES = {
 
 
 def sources_digest(label: str) -> str:
-    """Hash of the files that define the kernel behind `label`: its .cu file,
-    the shared device header and the C ABI header."""
+    """Hash of the files that define the kernel behind `label`: its .cu file
+    and the shared device header (the C ABI header only declares)."""
     import hashlib
     own = next(v for k, v in KERNEL_SOURCES.items() if label.startswith(k))
-    files = own + ["window_gather_swin_gb300/csrc/wgs_common.cuh", "include/wgs.h"]
+    files = own + ["window_gather_swin_gb300/csrc/wgs_common.cuh"]
     h = hashlib.sha256()
     for rel in files:
         with open(os.path.join(ROOT, rel), "rb") as f:

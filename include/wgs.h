@@ -60,7 +60,7 @@ typedef enum {
     WGS_ERR_CUDA = 10    /* another CUDA runtime call failed                */
 } wgs_status;
 
-typedef enum { WGS_F32 = 0, WGS_F16 = 1 } wgs_dtype;
+typedef enum { WGS_F32 = 0, WGS_F16 = 1, WGS_BF16 = 2 } wgs_dtype;
 
 /* Index-map construction order (wgs_build_window_index). */
 #define WGS_SHIFT_THEN_PAD 0
@@ -184,16 +184,42 @@ wgs_status residual_add_norm_gather(const void *residual, const void *branch, co
                                     int32_t width, float eps, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* bfloat16 forms of the LayerNorm family                               */
+/*      [P3 s3 and s12 list BF16 among the formats a hardened op covers] */
+/* ------------------------------------------------------------------ */
+/* Same arguments, rules and errors as the fp16 entry points above, with
+ * every 16-bit tensor in bfloat16: elements widen exactly to FP32, the
+ * statistics are FP32, and results round to nearest-even bfloat16.  The
+ * residual sum is round_bf16(fp32 a + fp32 b), which equals rounding the
+ * exact sum once (binary32 has at least 2 * 8 + 2 significand bits).
+ * window_gather copies rows bit for bit and serves both formats. */
+wgs_status ln_fwd_bf16(const void *x, void *y, int64_t rows, int32_t width, float eps,
+                       cudaStream_t stream);
+wgs_status residual_add_ln_fwd_bf16(const void *residual, const void *branch, void *residual_out,
+                                    void *y, int64_t rows, int32_t width, float eps,
+                                    cudaStream_t stream);
+wgs_status norm_gather_bf16(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                            int64_t n_idx, int32_t width, float eps, cudaStream_t stream);
+wgs_status window_reverse_add_ln_fwd_bf16(const void *residual, const void *windows,
+                                          const int32_t *inv_idx, void *residual_out, void *y,
+                                          int64_t rows, int64_t n_windowed, int32_t width,
+                                          float eps, cudaStream_t stream);
+wgs_status residual_add_norm_gather_bf16(const void *residual, const void *branch,
+                                         const int32_t *idx, void *residual_out, void *dst,
+                                         int64_t n_src, int64_t n_idx, int32_t width, float eps,
+                                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* bias_gelu_tanh -- fused bias + tanh-approximate GELU       [P3 s3] */
 /* ------------------------------------------------------------------ */
 /*     t = x + bias[col]   (rounded once to the tensor dtype)
  *     y = 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3)))
  * evaluated in FP32 and rounded to the tensor dtype.
- *   x, y   [rows, width] of `dtype` (WGS_F32 or WGS_F16); y == x allowed,
+ *   x, y   [rows, width] of `dtype` (WGS_F32, WGS_F16 or WGS_BF16); y == x allowed,
  *          other overlaps return WGS_ERR_ALIAS.
  *   bias   [width] of `dtype`; must not overlap y.
  *   width  any value >= 1.  A 16-byte vector path runs when width is a
- *          multiple of 4 (f32) or 8 (f16) and all pointers are 16-byte
+ *          multiple of 4 (f32) or 8 (16-bit types) and all pointers are 16-byte
  *          aligned; otherwise a scalar path runs (same results). */
 wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows, int32_t width,
                           wgs_dtype dtype, cudaStream_t stream);

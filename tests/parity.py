@@ -111,3 +111,42 @@ def check_gelu_f32(gpu: np.ndarray, y64: np.ndarray, what: str) -> dict:
              "violations": int((err > lim).sum())}
     assert stats["violations"] == 0, f"{what}: {stats}"
     return stats
+
+
+# ------------------------------------------------------------ bfloat16 ----
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).astype(np.int16)).view(
+        torch.bfloat16).double().numpy()
+
+
+def bf16_spacing(v: np.ndarray) -> np.ndarray:
+    """Distance from |v| to the next larger bfloat16 value (2^-133 below 2^-126)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7.0)
+
+
+def check_bf16_near(gpu_bits: np.ndarray, o_bits: np.ndarray, y64: np.ndarray, what: str,
+                    tie_abs: float = GELU_TIE_ABS) -> dict:
+    """bfloat16 outputs (bit patterns) against the oracle: the same FP32
+    error bound as for fp16, with bfloat16's spacing."""
+    g, o = bf16_values(gpu_bits), bf16_values(o_bits)
+    assert g.shape == o.shape == y64.shape, what
+    assert np.array_equal(np.isnan(g), np.isnan(o)), f"{what}: NaN positions differ"
+    fin = np.isfinite(o)
+    assert np.array_equal(g[~fin & ~np.isnan(o)], o[~fin & ~np.isnan(o)]), f"{what}: infinities"
+    g, o, y = g[fin], o[fin], y64[fin]
+    dist = ulp_distance(np.asarray(gpu_bits)[fin].view(np.float16), np.asarray(o_bits)[fin].view(np.float16))
+    err = np.abs(g - y)
+    bound = 0.5 * bf16_spacing(g) + TIE_REL * np.abs(y) + tie_abs
+    viol = err > bound
+    stats = {"n": int(g.size), "mismatches": int((dist > 0).sum()), "max_ulp": int(dist.max(initial=0)),
+             "max_abs": float(np.abs(g - o).max(initial=0.0)),
+             "max_err_over_bound": float((err / bound).max(initial=0.0))}
+    if viol.any():
+        k = np.argmax(err - bound)
+        raise AssertionError(f"{what}: {int(viol.sum())} elements outside the FP32 error bound, "
+                             f"worst gpu={g[k]!r} oracle={y[k]!r}; {stats}")
+    return stats

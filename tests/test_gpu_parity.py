@@ -469,6 +469,69 @@ def test_python_contract_errors():
     assert wgs.window_gather(x, torch.zeros(0, dtype=torch.int32, device=DEV)).shape == (0, 192)
 
 
+# ------------------------------------------------------------ bfloat16 ----
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("stage", [synth.TINY_PADDED, synth.STAGE_192, synth.STAGE_384],
+                         ids=lambda s: s.name)
+def test_bf16_layernorm_family(stage):
+    from parity import LN_TIE_ABS, check_bf16_near
+    bf = torch.bfloat16
+    n, c = stage.tokens, stage.width
+    x = synth.ln_input(n, c, seed=31, dtype=bf)
+    y = wgs.ln_fwd(x.to(DEV), EPS)
+    xb = _bits(x)
+    check_bf16_near(_bits(y), oracle.ln(xb, EPS, fmt="bf16"), oracle.ln_f64(xb, EPS, fmt="bf16"),
+                    "ln bf16", tie_abs=LN_TIE_ABS)
+
+    a, b = synth.residual_branch(n, c, seed=32, dtype=bf)
+    r, y = wgs.residual_add_ln_fwd(a.to(DEV), b.to(DEV), EPS)
+    o_r, o_y = oracle.residual_add_ln(_bits(a), _bits(b), EPS, fmt="bf16")
+    assert np.array_equal(_bits(r), o_r)
+    check_bf16_near(_bits(y), o_y, oracle.ln_f64(o_r, EPS, fmt="bf16"), "add+ln bf16",
+                    tie_abs=LN_TIE_ABS)
+
+    m = window_map(stage)
+    om = oracle_map(stage)
+    src = synth.gather_source(n, c, seed=33, dtype=bf)
+    g = wgs.norm_gather(src.to(DEV), m.to(DEV), EPS)
+    o_g, bad = oracle.norm_gather(_bits(src), om, EPS, fmt="bf16")
+    y64 = oracle.ln_f64(_bits(src), EPS, fmt="bf16")
+    want64 = np.where((om >= 0)[:, None], y64[np.maximum(om, 0)], 0.0)
+    check_bf16_near(_bits(g), o_g, want64, "norm_gather bf16", tie_abs=LN_TIE_ABS)
+    assert not _bits(g)[om < 0].any()
+    w = wgs.window_gather(src.to(DEV), m.to(DEV))          # bitwise, any 2-byte type
+    o_w, _ = oracle.window_gather(_bits(src).view(np.float16), om)
+    assert np.array_equal(_bits(w), o_w.view(np.uint16))
+
+    inv = wgs.build_window_inverse(stage.grid, synth.WINDOW, synth.SHIFT, stage.padded)
+    windows = synth.gather_source(m.numel(), c, seed=34, dtype=bf)
+    r, y = wgs.window_reverse_add_ln_fwd(a.to(DEV), windows.to(DEV), inv.to(DEV), EPS)
+    o_r, o_y, bad = oracle.window_reverse_add_ln(_bits(a), _bits(windows), om, EPS, fmt="bf16")
+    assert bad == 0 and np.array_equal(_bits(r), o_r)
+    check_bf16_near(_bits(y), o_y, oracle.ln_f64(o_r, EPS, fmt="bf16"), "reverse bf16",
+                    tie_abs=LN_TIE_ABS)
+
+    r, d = wgs.residual_add_norm_gather(a.to(DEV), b.to(DEV), m.to(DEV), EPS)
+    o_r, o_d, bad = oracle.residual_add_norm_gather(_bits(a), _bits(b), om, EPS, fmt="bf16")
+    assert bad == 0 and np.array_equal(_bits(r), o_r)
+    y64 = oracle.ln_f64(o_r, EPS, fmt="bf16")
+    want64 = np.where((om >= 0)[:, None], y64[np.maximum(om, 0)], 0.0)
+    check_bf16_near(_bits(d), o_d, want64, "add+norm+gather bf16", tie_abs=LN_TIE_ABS)
+
+
+@pytest.mark.parametrize("rows,width", [(32760, 1536), (5, 3), (17, 1000), (64, 768)])
+def test_bf16_gelu(rows, width):
+    from parity import check_bf16_near
+    x, b = synth.gelu_input(rows, width, torch.bfloat16, seed=rows)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    o, y64 = oracle.bias_gelu_tanh(_bits(x), _bits(b), fmt="bf16")
+    print("gelu bf16", check_bf16_near(_bits(y), o, y64, f"gelu bf16 {rows}x{width}"))
+
+
 # ------------------------------------------------------- graph capture ----
 
 def test_identical_results_when_captured_in_a_cuda_graph():

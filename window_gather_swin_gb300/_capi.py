@@ -16,7 +16,7 @@ STATUS_NAMES = {
     4: "WGS_ERR_ALIGN", 5: "WGS_ERR_DTYPE", 6: "WGS_ERR_ARCH", 7: "WGS_ERR_LAUNCH",
     8: "WGS_ERR_INDEX", 9: "WGS_ERR_ALIAS", 10: "WGS_ERR_CUDA",
 }
-WGS_F32, WGS_F16 = 0, 1
+WGS_F32, WGS_F16, WGS_BF16 = 0, 1, 2
 
 _P = ctypes.c_void_p
 _i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
@@ -34,6 +34,11 @@ SIGNATURES = {
     "window_reverse_add_ln_fwd": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "residual_add_norm_gather": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "wgs_build_window_inverse": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
+    "ln_fwd_bf16": (_st, [_P, _P, _i64, _i32, _f32, _P]),
+    "residual_add_ln_fwd_bf16": (_st, [_P, _P, _P, _P, _i64, _i32, _f32, _P]),
+    "norm_gather_bf16": (_st, [_P, _P, _P, _i64, _i64, _i32, _f32, _P]),
+    "window_reverse_add_ln_fwd_bf16": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
+    "residual_add_norm_gather_bf16": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "wgs_window_index_count": (_i64, [_P, _P, _P]),
     "wgs_build_window_index": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
     "wgs_check_error": (_st, [_P]),

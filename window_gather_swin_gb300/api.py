@@ -15,8 +15,20 @@ import torch
 
 from . import _capi
 
-_DTYPE = {torch.float32: _capi.WGS_F32, torch.float16: _capi.WGS_F16}
+_DTYPE = {torch.float32: _capi.WGS_F32, torch.float16: _capi.WGS_F16,
+          torch.bfloat16: _capi.WGS_BF16}
 LN_WIDTHS = (192, 384)
+ROW_DTYPES = (torch.float16, torch.bfloat16)
+
+
+def _entry(name: str, dtype):
+    """The C entry point for a 16-bit row op: fp16 `name`, bfloat16 `name_bf16`."""
+    return getattr(_capi.load(), name if dtype == torch.float16 else name + "_bf16")
+
+
+def _row16(t: torch.Tensor, name: str) -> None:
+    _cuda(t, name)
+    _require(t.dtype in ROW_DTYPES, f"{name} must be float16 or bfloat16 (got {t.dtype})")
 
 
 def _require(cond: bool, msg: str) -> None:
@@ -64,15 +76,16 @@ def _rows_width(x: torch.Tensor, name: str):
 # ------------------------------------------------------------------ LN ----
 
 def ln_fwd(x: torch.Tensor, eps: float = 1e-5, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """No-affine LayerNorm over the last dim (192 or 384) of an fp16 tensor."""
-    _cuda(x, "x", torch.float16)
+    """No-affine LayerNorm over the last dim (192 or 384) of an fp16 or
+    bfloat16 tensor."""
+    _row16(x, "x")
     rows, width = _rows_width(x, "x")
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
-    y = _out(out, x.shape, torch.float16, x.device, "out")
+    y = _out(out, x.shape, x.dtype, x.device, "out")
     _same_device(x, y)
     with torch.cuda.device(x.device):
-        _capi.check("ln_fwd", _capi.load().ln_fwd(_ptr(x), _ptr(y), rows, width, float(eps),
-                                                  _stream_ptr(x.device)))
+        _capi.check("ln_fwd", _entry("ln_fwd", x.dtype)(_ptr(x), _ptr(y), rows, width, float(eps),
+                                                        _stream_ptr(x.device)))
     return y
 
 
@@ -81,16 +94,16 @@ def residual_add_ln_fwd(residual: torch.Tensor, branch: torch.Tensor, eps: float
                         out: Optional[torch.Tensor] = None):
     """Returns (residual_out, y): residual_out = fp16(residual + branch),
     y = LN(residual_out)."""
-    _cuda(residual, "residual", torch.float16)
-    _cuda(branch, "branch", torch.float16)
+    _row16(residual, "residual")
+    _cuda(branch, "branch", residual.dtype)
     _require(residual.shape == branch.shape, "residual and branch must have the same shape")
     rows, width = _rows_width(residual, "residual")
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
-    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
-    y = _out(out, residual.shape, torch.float16, residual.device, "out")
+    r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
+    y = _out(out, residual.shape, residual.dtype, residual.device, "out")
     _same_device(residual, branch, r, y)
     with torch.cuda.device(residual.device):
-        _capi.check("residual_add_ln_fwd", _capi.load().residual_add_ln_fwd(
+        _capi.check("residual_add_ln_fwd", _entry("residual_add_ln_fwd", residual.dtype)(
             _ptr(residual), _ptr(branch), _ptr(r), _ptr(y), rows, width, float(eps),
             _stream_ptr(residual.device)))
     return r, y
@@ -99,19 +112,20 @@ def residual_add_ln_fwd(residual: torch.Tensor, branch: torch.Tensor, eps: float
 # -------------------------------------------------------------- gather ----
 
 def _gather_args(src, idx, out, name):
-    _cuda(src, "src", torch.float16)
+    _row16(src, "src")
     _cuda(idx, "idx", torch.int32)
     _require(src.dim() == 2, "src must be [n_src, width]")
     _require(idx.dim() == 1, "idx must be 1-D")
     n_src, width = src.shape
-    dst = _out(out, (idx.numel(), width), torch.float16, src.device, "out")
+    dst = _out(out, (idx.numel(), width), src.dtype, src.device, "out")
     _same_device(src, idx, dst)
     return n_src, width, dst
 
 
 def window_gather(src: torch.Tensor, idx: torch.Tensor,
                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """dst[d] = src[idx[d]] (idx >= 0) or a zero row (idx == -1)."""
+    """dst[d] = src[idx[d]] (idx >= 0) or a zero row (idx == -1).  Rows are
+    copied bit for bit, so fp16 and bfloat16 use the same kernel."""
     n_src, width, dst = _gather_args(src, idx, out, "window_gather")
     with torch.cuda.device(src.device):
         _capi.check("window_gather", _capi.load().window_gather(
@@ -125,7 +139,7 @@ def norm_gather(src: torch.Tensor, idx: torch.Tensor, eps: float = 1e-5,
     n_src, width, dst = _gather_args(src, idx, out, "norm_gather")
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
     with torch.cuda.device(src.device):
-        _capi.check("norm_gather", _capi.load().norm_gather(
+        _capi.check("norm_gather", _entry("norm_gather", src.dtype)(
             _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, float(eps),
             _stream_ptr(src.device)))
     return dst
@@ -139,19 +153,19 @@ def window_reverse_add_ln_fwd(residual: torch.Tensor, windows: torch.Tensor,
                               out: Optional[torch.Tensor] = None):
     """Returns (residual_out, y): residual_out[t] = fp16(residual[t] +
     windows[inv_idx[t]]), y = LN(residual_out)."""
-    _cuda(residual, "residual", torch.float16)
-    _cuda(windows, "windows", torch.float16)
+    _row16(residual, "residual")
+    _cuda(windows, "windows", residual.dtype)
     _cuda(inv_idx, "inv_idx", torch.int32)
     _require(residual.dim() == 2 and windows.dim() == 2, "residual and windows must be 2-D")
     rows, width = residual.shape
     _require(windows.shape[1] == width, "windows must have the residual's width")
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
     _require(inv_idx.dim() == 1 and inv_idx.numel() == rows, "inv_idx must have one entry per row")
-    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
-    y = _out(out, residual.shape, torch.float16, residual.device, "out")
+    r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
+    y = _out(out, residual.shape, residual.dtype, residual.device, "out")
     _same_device(residual, windows, inv_idx, r, y)
     with torch.cuda.device(residual.device):
-        _capi.check("window_reverse_add_ln_fwd", _capi.load().window_reverse_add_ln_fwd(
+        _capi.check("window_reverse_add_ln_fwd", _entry("window_reverse_add_ln_fwd", residual.dtype)(
             _ptr(residual), _ptr(windows), _ptr(inv_idx), _ptr(r), _ptr(y), rows,
             windows.shape[0], width, float(eps), _stream_ptr(residual.device)))
     return r, y
@@ -162,19 +176,19 @@ def residual_add_norm_gather(residual: torch.Tensor, branch: torch.Tensor, idx: 
                              out: Optional[torch.Tensor] = None):
     """Returns (residual_out, dst): residual_out = fp16(residual + branch),
     dst[d] = LN(residual_out)[idx[d]] (zero row for -1)."""
-    _cuda(residual, "residual", torch.float16)
-    _cuda(branch, "branch", torch.float16)
+    _row16(residual, "residual")
+    _cuda(branch, "branch", residual.dtype)
     _cuda(idx, "idx", torch.int32)
     _require(residual.shape == branch.shape and residual.dim() == 2,
              "residual and branch must be 2-D and of the same shape")
     n_src, width = residual.shape
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
     _require(idx.dim() == 1, "idx must be 1-D")
-    r = _out(residual_out, residual.shape, torch.float16, residual.device, "residual_out")
-    dst = _out(out, (idx.numel(), width), torch.float16, residual.device, "out")
+    r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
+    dst = _out(out, (idx.numel(), width), residual.dtype, residual.device, "out")
     _same_device(residual, branch, idx, r, dst)
     with torch.cuda.device(residual.device):
-        _capi.check("residual_add_norm_gather", _capi.load().residual_add_norm_gather(
+        _capi.check("residual_add_norm_gather", _entry("residual_add_norm_gather", residual.dtype)(
             _ptr(residual), _ptr(branch), _ptr(idx), _ptr(r), _ptr(dst), n_src, idx.numel(), width,
             float(eps), _stream_ptr(residual.device)))
     return r, dst
@@ -184,9 +198,9 @@ def residual_add_norm_gather(residual: torch.Tensor, branch: torch.Tensor, idx: 
 
 def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """gelu_tanh(x + bias) over the last dim, fp32 or fp16."""
+    """gelu_tanh(x + bias) over the last dim, fp32, fp16 or bfloat16."""
     _cuda(x, "x")
-    _require(x.dtype in _DTYPE, f"x must be float32 or float16 (got {x.dtype})")
+    _require(x.dtype in _DTYPE, f"x must be float32, float16 or bfloat16 (got {x.dtype})")
     _cuda(bias, "bias", x.dtype)
     _require(x.dim() >= 1, "x must have at least one dimension")
     width = x.shape[-1]

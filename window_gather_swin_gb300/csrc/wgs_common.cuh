@@ -1,6 +1,7 @@
 // Shared host and device helpers of the sm_103a block-glue kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -113,6 +114,43 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int j) {
 __device__ __forceinline__ void set_word(uint4 &v, int j, uint32_t w) {
     if (j == 0) v.x = w; else if (j == 1) v.y = w; else if (j == 2) v.z = w; else v.w = w;
 }
+
+// 16-bit element formats of the row kernels: two elements per 32-bit word.
+// to_f2 widens exactly; from_f2 rounds to nearest even; add2 returns
+// round(a + b) for each pair, which for both formats equals rounding the
+// binary32 sum once more (binary32 carries at least 2p + 2 bits for a
+// p-bit format, so the double rounding is innocuous).
+struct Fp16 {
+    __device__ static float2 to_f2(uint32_t w) { return half2_to_float2(w); }
+    __device__ static uint32_t from_f2(float a, float b) { return float2_to_half2(a, b); }
+    __device__ static uint32_t add2(uint32_t a, uint32_t b) {
+        __half2 x, y;
+        memcpy(&x, &a, 4);
+        memcpy(&y, &b, 4);
+        const __half2 z = __hadd2(x, y);
+        uint32_t r;
+        memcpy(&r, &z, 4);
+        return r;
+    }
+};
+
+struct Bf16 {
+    __device__ static float2 to_f2(uint32_t w) {
+        __nv_bfloat162 h;
+        memcpy(&h, &w, 4);
+        return __bfloat1622float2(h);
+    }
+    __device__ static uint32_t from_f2(float a, float b) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        uint32_t r;
+        memcpy(&r, &h, 4);
+        return r;
+    }
+    __device__ static uint32_t add2(uint32_t a, uint32_t b) {
+        const float2 x = to_f2(a), y = to_f2(b);
+        return from_f2(x.x + y.x, x.y + y.y);
+    }
+};
 
 // Sum over the LPR consecutive lanes that share a row (LPR a power of two,
 // groups aligned to LPR), by butterfly exchange; every lane of the group

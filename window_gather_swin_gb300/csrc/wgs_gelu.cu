@@ -24,6 +24,7 @@
 // moves 16-byte chunks and keeps U independent chunks in flight per thread.
 // Bias chunks come through L1 (the whole bias row is at most a few KB).
 #include <atomic>
+#include <type_traits>
 
 #include "wgs_common.cuh"
 
@@ -79,25 +80,24 @@ __device__ __forceinline__ float gelu_tanh(float t) {
     return t < kFarLeft ? gelu_tanh_far_left(t) : gelu_tanh_fast(t);
 }
 
-// One 16-byte chunk: 4 fp32 or 8 fp16 elements and the matching bias chunk.
-// The fast formula runs on every element; the rare far-left elements are
-// redone afterwards behind one branch per chunk.
-template <bool kHalf>
+// Element formats: F32 here, Fp16 / Bf16 from wgs_common.cuh.
+struct F32 {};
+
+// One 16-byte chunk: 4 fp32 or 8 16-bit elements and the matching bias
+// chunk.  The fast formula runs on every element; the rare far-left
+// elements are redone afterwards behind one branch per chunk.
+template <typename E>
 __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
-    constexpr int kN = kHalf ? 8 : 4;
+    constexpr bool k16 = !std::is_same<E, F32>::value;
+    constexpr int kN = k16 ? 8 : 4;
     float t[kN], y[kN];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if constexpr (kHalf) {
-            // t = fp16(x + b): one correctly rounded fp16 add, equal to
-            // fp16(fp32 x + fp32 b) because binary32 holds the sum of two
-            // binary16 values to within a rounding that cannot move it
-            // across an fp16 rounding boundary (24 >= 2 * 11 + 2).
-            __half2 xh, bh;
-            const uint32_t xw = word(xv, j), bw = word(bv, j);
-            memcpy(&xh, &xw, 4);
-            memcpy(&bh, &bw, 4);
-            const float2 tf = __half22float2(__hadd2(xh, bh));
+        if constexpr (k16) {
+            // t = round(x + b) in the tensor's 16-bit format, the rounding
+            // point of an unfused add in that precision (E::add2 rounds the
+            // exact sum once)
+            const float2 tf = E::to_f2(E::add2(word(xv, j), word(bv, j)));
             t[2 * j] = tf.x;
             t[2 * j + 1] = tf.y;
         } else {
@@ -118,8 +118,8 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
     uint4 out;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if constexpr (kHalf)
-            set_word(out, j, float2_to_half2(y[2 * j], y[2 * j + 1]));
+        if constexpr (k16)
+            set_word(out, j, E::from_f2(y[2 * j], y[2 * j + 1]));
         else
             set_word(out, j, __float_as_uint(y[j]));
     }
@@ -129,7 +129,7 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
 // Flat grid-stride over 16-byte chunks.  Chunk i belongs to column chunk
 // i mod row_vecs; each thread tracks that column incrementally (all steps
 // are below row_vecs, so one conditional subtraction keeps it in range).
-template <bool kHalf, int U, int THREADS>
+template <typename E, int U, int THREADS>
 __global__ void WGS_GELU_BOUNDS(THREADS)
 bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec, int32_t row_vecs) {
     pdl_prologue();
@@ -155,7 +155,7 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
-            if (i < n_vec) st_stream(y + i, gelu_chunk<kHalf>(xv[u], bv[u]));
+            if (i < n_vec) st_stream(y + i, gelu_chunk<E>(xv[u], bv[u]));
         }
         col0 += per_iter;
         if (col0 >= row_vecs) col0 -= row_vecs;
@@ -163,30 +163,31 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
 }
 
 // Any width, any element alignment: one element per thread per step.
-template <bool kHalf>
+template <typename E>
 __global__ void __launch_bounds__(256)
 bias_gelu_scalar_kernel(const void *xp, const void *bp, void *yp, int64_t n, int32_t width) {
     pdl_prologue();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int32_t c = static_cast<int32_t>(i % width);
-        if constexpr (kHalf) {
-            const __half *x = static_cast<const __half *>(xp);
-            const __half *b = static_cast<const __half *>(bp);
-            const __half t = __float2half_rn(__half2float(x[i]) + __half2float(b[c]));
-            static_cast<__half *>(yp)[i] = __float2half_rn(gelu_tanh(__half2float(t)));
-        } else {
+        if constexpr (std::is_same<E, F32>::value) {
             const float *x = static_cast<const float *>(xp);
             const float *b = static_cast<const float *>(bp);
             static_cast<float *>(yp)[i] = gelu_tanh(x[i] + b[c]);
+        } else {
+            // one 16-bit element in the low half of a word
+            const uint16_t *x = static_cast<const uint16_t *>(xp);
+            const uint16_t *b = static_cast<const uint16_t *>(bp);
+            const float t = E::to_f2(E::add2(x[i], b[c])).x;
+            static_cast<uint16_t *>(yp)[i] = static_cast<uint16_t>(E::from_f2(gelu_tanh(t), 0.f));
         }
     }
 }
 
-template <bool kHalf>
+template <typename E>
 wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, int32_t width,
                        int device, int sm_count, cudaStream_t stream) {
-    constexpr int kVec = kHalf ? 8 : 4;
+    constexpr int kVec = std::is_same<E, F32>::value ? 4 : 8;
     const int64_t n = rows * width;
     const bool vec = width % kVec == 0 && aligned16(x) && aligned16(bias) && aligned16(y);
     if (vec) {
@@ -195,7 +196,7 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
         const int64_t need = ceil_div(n_vec, static_cast<int64_t>(T) * U);
         // One resident wave of grid-stride CTAs: a partial second wave
         // would leave SMs idle at the end of this bandwidth-bound stream.
-        auto kernel = bias_gelu_vec_kernel<kHalf, U, T>;
+        auto kernel = bias_gelu_vec_kernel<E, U, T>;
         static std::atomic<int> resident[64];  // per device, for this instantiation
         int per_sm = WGS_GELU_CTAS_PER_SM > 0 ? WGS_GELU_CTAS_PER_SM
                                               : resident[device].load(std::memory_order_relaxed);
@@ -213,7 +214,7 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
     }
     const int64_t need = ceil_div(n, 256);
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-    return launch(bias_gelu_scalar_kernel<kHalf>, dim3(static_cast<unsigned>(need < cap ? need : cap)),
+    return launch(bias_gelu_scalar_kernel<E>, dim3(static_cast<unsigned>(need < cap ? need : cap)),
                   dim3(256), 0, stream, x, bias, y, n, width);
 }
 
@@ -223,7 +224,7 @@ using namespace wgs;
 
 extern "C" wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows,
                                      int32_t width, wgs_dtype dtype, cudaStream_t stream) {
-    if (dtype != WGS_F32 && dtype != WGS_F16) return WGS_ERR_DTYPE;
+    if (dtype != WGS_F32 && dtype != WGS_F16 && dtype != WGS_BF16) return WGS_ERR_DTYPE;
     if (rows < 0 || width < 0) return WGS_ERR_SHAPE;
     const int64_t esz = dtype == WGS_F32 ? 4 : 2;
     if (width > 0 && rows > INT64_MAX / esz / width) return WGS_ERR_SHAPE;
@@ -238,7 +239,12 @@ extern "C" wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, i
     DeviceInfo dev;
     const wgs_status st = current_device(&dev);
     if (st != WGS_OK) return st;
-    return dtype == WGS_F16
-               ? launch_gelu<true>(x, bias, y, rows, width, dev.device, dev.sm_count, stream)
-               : launch_gelu<false>(x, bias, y, rows, width, dev.device, dev.sm_count, stream);
+    switch (dtype) {
+        case WGS_F16:
+            return launch_gelu<Fp16>(x, bias, y, rows, width, dev.device, dev.sm_count, stream);
+        case WGS_BF16:
+            return launch_gelu<Bf16>(x, bias, y, rows, width, dev.device, dev.sm_count, stream);
+        default:
+            return launch_gelu<F32>(x, bias, y, rows, width, dev.device, dev.sm_count, stream);
+    }
 }

@@ -42,10 +42,10 @@ __device__ unsigned int g_index_error;
 enum class RowOp : int { kLN, kAddLN, kGather, kNormGather, kRevAddLN, kAddNormGather };
 
 struct RowArgs {
-    const __half *in0;    // x / residual / src
-    const __half *in1;    // branch (add + LN, add + norm + gather), windows (reverse)
-    __half *out0;         // y (LN, gathers) or residual_out (the add ops)
-    __half *out1;         // y / dst of the add ops
+    const uint16_t *in0;  // x / residual / src (16-bit elements)
+    const uint16_t *in1;  // branch (add + LN, add + norm + gather), windows (reverse)
+    uint16_t *out0;       // y (LN, gathers) or residual_out (the add ops)
+    uint16_t *out1;       // y / dst of the add ops
     const int32_t *idx;   // window map (gathers) or its inverse (reverse)
     int64_t rows;         // rows of the launch: tokens, or windowed rows for the gathers
     int64_t n_src;        // bound of idx values: source rows, or windowed rows (reverse)
@@ -76,22 +76,22 @@ template <> struct RowTiling<384> { static constexpr int kLPR = WGS_LPR384; };
 // saves the long correctly rounded divide / square-root sequences once per
 // row.  Every LN kernel calls this one function, so equal inputs give
 // equal bits.
-template <int WIDTH, int LPR, int CPL, int U>
+template <typename E, int WIDTH, int LPR, int CPL, int U>
 __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
-    constexpr int E = CPL * 8;  // elements of one row held by this lane
+    constexpr int NE = CPL * 8;  // elements of one row held by this lane
     constexpr float kInvWidth = 1.0f / WIDTH;
     const int lead = (threadIdx.x & 31) & ~(LPR - 1);  // lane holding the row's first chunk
-    float d[U][E];
+    float d[U][NE];
     float mean[U], rstd[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const float shift = __shfl_sync(0xffffffffu, half2_to_float2(v[u][0].x).x, lead);
+        const float shift = __shfl_sync(0xffffffffu, E::to_f2(v[u][0].x).x, lead);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 f = half2_to_float2(word(v[u][c], j));
+                const float2 f = E::to_f2(word(v[u][c], j));
                 d[u][c * 8 + 2 * j] = f.x - shift;
                 d[u][c * 8 + 2 * j + 1] = f.y - shift;
                 acc[j] += d[u][c * 8 + 2 * j];
@@ -105,7 +105,7 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
     for (int u = 0; u < U; ++u) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
+        for (int e = 0; e < NE; ++e) {
             d[u][e] -= mean[u];
             acc[e & 3] = fmaf(d[u][e], d[u][e], acc[e & 3]);
         }
@@ -123,31 +123,19 @@ __device__ __forceinline__ void ln_normalize(uint4 (&v)[U][CPL], float eps) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 set_word(v[u][c], j,
-                         float2_to_half2(d[u][c * 8 + 2 * j] * rstd[u],
-                                         d[u][c * 8 + 2 * j + 1] * rstd[u]));
+                         E::from_f2(d[u][c * 8 + 2 * j] * rstd[u], d[u][c * 8 + 2 * j + 1] * rstd[u]));
 }
 
-// residual_out = fp16(residual + branch) on one 16-byte chunk.  A binary16
-// add rounds the exact sum once, which equals fp16(fp32 a + fp32 b) because
-// binary32 holds the sum closely enough (24 >= 2 * 11 + 2) that the second
-// rounding never crosses an fp16 rounding boundary.
-__device__ __forceinline__ uint4 add_fp16_chunk(const uint4 &a, const uint4 &b) {
+// residual_out = round(residual + branch) on one 16-byte chunk.
+template <typename E>
+__device__ __forceinline__ uint4 add_chunk(const uint4 &a, const uint4 &b) {
     uint4 r;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        __half2 x, y;
-        const uint32_t xa = word(a, j), yb = word(b, j);
-        memcpy(&x, &xa, 4);
-        memcpy(&y, &yb, 4);
-        const __half2 z = __hadd2(x, y);
-        uint32_t zb;
-        memcpy(&zb, &z, 4);
-        set_word(r, j, zb);
-    }
+    for (int j = 0; j < 4; ++j) set_word(r, j, E::add2(word(a, j), word(b, j)));
     return r;
 }
 
-template <RowOp OP, int WIDTH, int U, int WARPS>
+template <RowOp OP, typename E, int WIDTH, int U, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
     pdl_prologue();
     constexpr int LPR = RowTiling<WIDTH>::kLPR;
@@ -223,7 +211,7 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
             for (int u = 0; u < U; ++u)
                 if (branch[u])
 #pragma unroll
-                    for (int k = 0; k < CPL; ++k) v[u][k] = add_fp16_chunk(v[u][k], b[u][k]);
+                    for (int k = 0; k < CPL; ++k) v[u][k] = add_chunk<E>(v[u][k], b[u][k]);
             // the residual stream is written at its own (source) row
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -233,9 +221,9 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
                         st_stream(a.out0 + src[u] * WIDTH + (sub + k * LPR) * 8, v[u][k]);
         }
 
-        if constexpr (kNorm) ln_normalize<WIDTH, LPR, CPL, U>(v, a.eps);
+        if constexpr (kNorm) ln_normalize<E, WIDTH, LPR, CPL, U>(v, a.eps);
 
-        __half *out = kTwoInputs ? a.out1 : a.out0;
+        uint16_t *out = kTwoInputs ? a.out1 : a.out0;
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (live[u])
@@ -264,7 +252,7 @@ __global__ void __launch_bounds__(256) gather_any_width_kernel(const uint4 *src,
     }
 }
 
-template <RowOp OP, int WIDTH>
+template <RowOp OP, typename E, int WIDTH>
 wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     DeviceInfo dev;
     const wgs_status st = current_device(&dev);
@@ -274,24 +262,25 @@ wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     const int64_t iters = ceil_div(a.rows, ROWS_CTA);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
     const unsigned grid = static_cast<unsigned>(iters < cap ? iters : cap);
-    return launch(row_kernel<OP, WIDTH, U, WARPS>, dim3(grid), dim3(WARPS * 32), 0, stream, a);
+    return launch(row_kernel<OP, E, WIDTH, U, WARPS>, dim3(grid), dim3(WARPS * 32), 0, stream, a);
 }
 
-template <RowOp OP>
+template <RowOp OP, typename E = Fp16>
 wgs_status dispatch_width(const RowArgs &a, int32_t width, cudaStream_t stream) {
-    return width == 192 ? launch_rows<OP, 192>(a, stream) : launch_rows<OP, 384>(a, stream);
+    return width == 192 ? launch_rows<OP, E, 192>(a, stream) : launch_rows<OP, E, 384>(a, stream);
 }
 
 bool ln_width(int32_t width) { return width == 192 || width == 384; }
 
-// rows * width fp16 values must be addressable in bytes.
+// rows * width 16-bit values must be addressable in bytes.
 bool fits(int64_t rows, int32_t width) { return rows <= INT64_MAX / 2 / width; }
 
 }  // namespace wgs
 
 using namespace wgs;
 
-extern "C" wgs_status ln_fwd(const void *x, void *y, int64_t rows, int32_t width, float eps,
+template <typename E>
+wgs_status ln_fwd_impl(const void *x, void *y, int64_t rows, int32_t width, float eps,
                              cudaStream_t stream) {
     if (!ln_width(width)) return WGS_ERR_WIDTH;
     if (rows < 0 || !fits(rows, width)) return WGS_ERR_SHAPE;
@@ -300,12 +289,13 @@ extern "C" wgs_status ln_fwd(const void *x, void *y, int64_t rows, int32_t width
     if (!aligned16(x) || !aligned16(y)) return WGS_ERR_ALIGN;
     const int64_t bytes = rows * width * 2;
     if (!same_or_disjoint(x, y, bytes)) return WGS_ERR_ALIAS;
-    RowArgs a{static_cast<const __half *>(x), nullptr, static_cast<__half *>(y), nullptr,
+    RowArgs a{static_cast<const uint16_t *>(x), nullptr, static_cast<uint16_t *>(y), nullptr,
               nullptr, rows, 0, eps};
-    return dispatch_width<RowOp::kLN>(a, width, stream);
+    return dispatch_width<RowOp::kLN, E>(a, width, stream);
 }
 
-extern "C" wgs_status residual_add_ln_fwd(const void *residual, const void *branch,
+template <typename E>
+wgs_status residual_add_ln_fwd_impl(const void *residual, const void *branch,
                                           void *residual_out, void *y, int64_t rows,
                                           int32_t width, float eps, cudaStream_t stream) {
     if (!ln_width(width)) return WGS_ERR_WIDTH;
@@ -320,9 +310,9 @@ extern "C" wgs_status residual_add_ln_fwd(const void *residual, const void *bran
         !same_or_disjoint(residual_out, branch, bytes) || !same_or_disjoint(y, residual, bytes) ||
         !same_or_disjoint(y, branch, bytes))
         return WGS_ERR_ALIAS;
-    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(branch),
-              static_cast<__half *>(residual_out), static_cast<__half *>(y), nullptr, rows, 0, eps};
-    return dispatch_width<RowOp::kAddLN>(a, width, stream);
+    RowArgs a{static_cast<const uint16_t *>(residual), static_cast<const uint16_t *>(branch),
+              static_cast<uint16_t *>(residual_out), static_cast<uint16_t *>(y), nullptr, rows, 0, eps};
+    return dispatch_width<RowOp::kAddLN, E>(a, width, stream);
 }
 
 namespace {
@@ -346,7 +336,7 @@ extern "C" wgs_status window_gather(const void *src, const int32_t *idx, void *d
     if (width <= 0 || width % 8 != 0) return WGS_ERR_WIDTH;
     wgs_status st = check_gather(src, idx, dst, n_src, n_idx, width);
     if (st != WGS_OK || n_idx == 0) return st;
-    RowArgs a{static_cast<const __half *>(src), nullptr, static_cast<__half *>(dst), nullptr, idx,
+    RowArgs a{static_cast<const uint16_t *>(src), nullptr, static_cast<uint16_t *>(dst), nullptr, idx,
               n_idx, n_src, 0.f};
     if (ln_width(width)) return dispatch_width<RowOp::kGather>(a, width, stream);
 
@@ -361,17 +351,19 @@ extern "C" wgs_status window_gather(const void *src, const int32_t *idx, void *d
                   static_cast<uint4 *>(dst), n_src, n_idx, static_cast<int32_t>(width / 8));
 }
 
-extern "C" wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+template <typename E>
+wgs_status norm_gather_impl(const void *src, const int32_t *idx, void *dst, int64_t n_src,
                                   int64_t n_idx, int32_t width, float eps, cudaStream_t stream) {
     if (!ln_width(width)) return WGS_ERR_WIDTH;
     const wgs_status st = check_gather(src, idx, dst, n_src, n_idx, width);
     if (st != WGS_OK || n_idx == 0) return st;
-    RowArgs a{static_cast<const __half *>(src), nullptr, static_cast<__half *>(dst), nullptr, idx,
+    RowArgs a{static_cast<const uint16_t *>(src), nullptr, static_cast<uint16_t *>(dst), nullptr, idx,
               n_idx, n_src, eps};
-    return dispatch_width<RowOp::kNormGather>(a, width, stream);
+    return dispatch_width<RowOp::kNormGather, E>(a, width, stream);
 }
 
-extern "C" wgs_status window_reverse_add_ln_fwd(const void *residual, const void *windows,
+template <typename E>
+wgs_status window_reverse_add_ln_fwd_impl(const void *residual, const void *windows,
                                                 const int32_t *inv_idx, void *residual_out,
                                                 void *y, int64_t rows, int64_t n_windowed,
                                                 int32_t width, float eps, cudaStream_t stream) {
@@ -391,13 +383,14 @@ extern "C" wgs_status window_reverse_add_ln_fwd(const void *residual, const void
         overlap(windows, wbytes, y, bytes) || overlap(inv_idx, rows * 4, residual_out, bytes) ||
         overlap(inv_idx, rows * 4, y, bytes))
         return WGS_ERR_ALIAS;
-    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(windows),
-              static_cast<__half *>(residual_out), static_cast<__half *>(y), inv_idx, rows,
+    RowArgs a{static_cast<const uint16_t *>(residual), static_cast<const uint16_t *>(windows),
+              static_cast<uint16_t *>(residual_out), static_cast<uint16_t *>(y), inv_idx, rows,
               n_windowed, eps};
-    return dispatch_width<RowOp::kRevAddLN>(a, width, stream);
+    return dispatch_width<RowOp::kRevAddLN, E>(a, width, stream);
 }
 
-extern "C" wgs_status residual_add_norm_gather(const void *residual, const void *branch,
+template <typename E>
+wgs_status residual_add_norm_gather_impl(const void *residual, const void *branch,
                                                const int32_t *idx, void *residual_out, void *dst,
                                                int64_t n_src, int64_t n_idx, int32_t width,
                                                float eps, cudaStream_t stream) {
@@ -415,10 +408,78 @@ extern "C" wgs_status residual_add_norm_gather(const void *residual, const void 
         overlap(dst, dbytes, branch, bytes) || overlap(dst, dbytes, residual_out, bytes) ||
         overlap(idx, n_idx * 4, dst, dbytes) || overlap(idx, n_idx * 4, residual_out, bytes))
         return WGS_ERR_ALIAS;
-    RowArgs a{static_cast<const __half *>(residual), static_cast<const __half *>(branch),
-              static_cast<__half *>(residual_out), static_cast<__half *>(dst), idx, n_idx, n_src,
+    RowArgs a{static_cast<const uint16_t *>(residual), static_cast<const uint16_t *>(branch),
+              static_cast<uint16_t *>(residual_out), static_cast<uint16_t *>(dst), idx, n_idx, n_src,
               eps};
-    return dispatch_width<RowOp::kAddNormGather>(a, width, stream);
+    return dispatch_width<RowOp::kAddNormGather, E>(a, width, stream);
+}
+
+// ------------------------------------------------ C entry points ------
+// Each LayerNorm-family op has an fp16 and a bfloat16 entry point with the
+// same arguments; the format only changes how elements widen and round.
+
+extern "C" wgs_status ln_fwd(const void *x, void *y, int64_t rows, int32_t width, float eps,
+                             cudaStream_t stream) {
+    return ln_fwd_impl<Fp16>(x, y, rows, width, eps, stream);
+}
+extern "C" wgs_status ln_fwd_bf16(const void *x, void *y, int64_t rows, int32_t width, float eps,
+                                  cudaStream_t stream) {
+    return ln_fwd_impl<Bf16>(x, y, rows, width, eps, stream);
+}
+
+extern "C" wgs_status residual_add_ln_fwd(const void *residual, const void *branch,
+                                          void *residual_out, void *y, int64_t rows,
+                                          int32_t width, float eps, cudaStream_t stream) {
+    return residual_add_ln_fwd_impl<Fp16>(residual, branch, residual_out, y, rows, width, eps,
+                                          stream);
+}
+extern "C" wgs_status residual_add_ln_fwd_bf16(const void *residual, const void *branch,
+                                               void *residual_out, void *y, int64_t rows,
+                                               int32_t width, float eps, cudaStream_t stream) {
+    return residual_add_ln_fwd_impl<Bf16>(residual, branch, residual_out, y, rows, width, eps,
+                                          stream);
+}
+
+extern "C" wgs_status norm_gather(const void *src, const int32_t *idx, void *dst, int64_t n_src,
+                                  int64_t n_idx, int32_t width, float eps, cudaStream_t stream) {
+    return norm_gather_impl<Fp16>(src, idx, dst, n_src, n_idx, width, eps, stream);
+}
+extern "C" wgs_status norm_gather_bf16(const void *src, const int32_t *idx, void *dst,
+                                       int64_t n_src, int64_t n_idx, int32_t width, float eps,
+                                       cudaStream_t stream) {
+    return norm_gather_impl<Bf16>(src, idx, dst, n_src, n_idx, width, eps, stream);
+}
+
+extern "C" wgs_status window_reverse_add_ln_fwd(const void *residual, const void *windows,
+                                                const int32_t *inv_idx, void *residual_out,
+                                                void *y, int64_t rows, int64_t n_windowed,
+                                                int32_t width, float eps, cudaStream_t stream) {
+    return window_reverse_add_ln_fwd_impl<Fp16>(residual, windows, inv_idx, residual_out, y, rows,
+                                                n_windowed, width, eps, stream);
+}
+extern "C" wgs_status window_reverse_add_ln_fwd_bf16(const void *residual, const void *windows,
+                                                     const int32_t *inv_idx, void *residual_out,
+                                                     void *y, int64_t rows, int64_t n_windowed,
+                                                     int32_t width, float eps,
+                                                     cudaStream_t stream) {
+    return window_reverse_add_ln_fwd_impl<Bf16>(residual, windows, inv_idx, residual_out, y, rows,
+                                                n_windowed, width, eps, stream);
+}
+
+extern "C" wgs_status residual_add_norm_gather(const void *residual, const void *branch,
+                                               const int32_t *idx, void *residual_out, void *dst,
+                                               int64_t n_src, int64_t n_idx, int32_t width,
+                                               float eps, cudaStream_t stream) {
+    return residual_add_norm_gather_impl<Fp16>(residual, branch, idx, residual_out, dst, n_src,
+                                               n_idx, width, eps, stream);
+}
+extern "C" wgs_status residual_add_norm_gather_bf16(const void *residual, const void *branch,
+                                                    const int32_t *idx, void *residual_out,
+                                                    void *dst, int64_t n_src, int64_t n_idx,
+                                                    int32_t width, float eps,
+                                                    cudaStream_t stream) {
+    return residual_add_norm_gather_impl<Bf16>(residual, branch, idx, residual_out, dst, n_src,
+                                               n_idx, width, eps, stream);
 }
 
 extern "C" wgs_status wgs_check_error(cudaStream_t stream) {

@@ -59,26 +59,27 @@ def _gen(seed: int) -> torch.Generator:
     return g
 
 
-def ln_input(rows: int, width: int, seed: int = 1) -> torch.Tensor:
-    """fp16 [rows, width]: N(0,1) plus a per-row offset drawn from U(-4, 4)."""
+def ln_input(rows: int, width: int, seed: int = 1, dtype=torch.float16) -> torch.Tensor:
+    """[rows, width] (fp16 by default): N(0,1) plus a per-row offset drawn from U(-4, 4)."""
     g = _gen(seed)
     x = torch.randn(rows, width, generator=g, dtype=torch.float32)
     off = torch.rand(rows, 1, generator=g, dtype=torch.float32) * 8.0 - 4.0
-    return (x + off).to(torch.float16)
+    return (x + off).to(dtype)
 
 
-def residual_branch(rows: int, width: int, seed: int = 2, branch_std: float = 0.1):
-    """(residual, branch), fp16 [rows, width]: N(0,1) and N(0, branch_std)."""
+def residual_branch(rows: int, width: int, seed: int = 2, branch_std: float = 0.1,
+                    dtype=torch.float16):
+    """(residual, branch), [rows, width]: N(0,1) and N(0, branch_std)."""
     g = _gen(seed)
     a = torch.randn(rows, width, generator=g, dtype=torch.float32)
     b = torch.randn(rows, width, generator=g, dtype=torch.float32) * branch_std
-    return a.to(torch.float16), b.to(torch.float16)
+    return a.to(dtype), b.to(dtype)
 
 
-def gather_source(rows: int, width: int, seed: int = 3) -> torch.Tensor:
-    """fp16 [rows, width] ~ N(0,1)."""
+def gather_source(rows: int, width: int, seed: int = 3, dtype=torch.float16) -> torch.Tensor:
+    """[rows, width] ~ N(0,1)."""
     g = _gen(seed)
-    return torch.randn(rows, width, generator=g, dtype=torch.float32).to(torch.float16)
+    return torch.randn(rows, width, generator=g, dtype=torch.float32).to(dtype)
 
 
 def gelu_input(rows: int, width: int, dtype=torch.float32, seed: int = 4):
