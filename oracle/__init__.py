@@ -55,6 +55,7 @@ def _load():
             "orc_invert_window_index": (None, [P, i64, P, i64]),
             "orc_residual_add_norm_gather": (i64, [P, P, P, P, P, i64, i64, i32, f32]),
             "orc_bias_gelu_f32": (None, [P, P, P, P, i64, i32]),
+            "orc_bias_gelu_bwd": (None, [P, P, P, P, P, P, P, i64, i32, ctypes.c_int]),
             "orc_bias_gelu_f16": (None, [P, P, P, P, i64, i32]),
         }
         for name, (res, args) in sig.items():
@@ -272,3 +273,24 @@ def bias_gelu_tanh(x, bias, want_f64: bool = True, fmt: str = None):
     y = np.empty_like(xs)
     lib.orc_bias_gelu_16(_ptr(xs), _ptr(bs), _ptr(y), _ptr(y64), rows, width, code)
     return y, y64
+
+
+def bias_gelu_tanh_bwd(grad_y, x, bias, fmt: str = None):
+    """Backward of y = gelu_tanh(x + bias).  Returns (grad_x, grad_bias,
+    grad_x64, grad_bias64): the rounded results in the input format and the
+    unrounded double values.  float32 arrays by default; fmt="f16" takes
+    float16 arrays, fmt="bf16" uint16 bit patterns."""
+    x = np.asarray(x)
+    if fmt is None:
+        fmt = {np.dtype(np.float32): "f32", np.dtype(np.float16): "f16"}.get(x.dtype)
+    code, dt = {"f32": (-1, np.float32), "f16": (0, np.float16), "bf16": (1, np.uint16)}[fmt]
+    gy, xs, bs = _c(grad_y, dt), _c(x, dt), _c(bias, dt).ravel()
+    rows, width = xs.shape
+    assert gy.shape == xs.shape and bs.shape == (width,)
+    gx = np.empty_like(xs)
+    gb = np.empty(width, dtype=dt)
+    gx64 = np.empty(xs.shape, dtype=np.float64)
+    gb64 = np.empty(width, dtype=np.float64)
+    _load().orc_bias_gelu_bwd(_ptr(gy), _ptr(xs), _ptr(bs), _ptr(gx), _ptr(gb), _ptr(gx64),
+                              _ptr(gb64), rows, width, code)
+    return gx, gb, gx64, gb64

@@ -21,6 +21,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> double                                        */
@@ -517,4 +518,70 @@ int64_t orc_residual_add_norm_gather(const uint16_t *a, const uint16_t *b, const
                                      int64_t n_idx, int32_t width, float eps)
 {
     return orc_residual_add_norm_gather_fmt(a, b, idx, r_out, dst, n_src, n_idx, width, eps, 0);
+}
+
+/* ------------------------------------------------------------------ */
+/* Backward of bias + tanh-GELU                                        */
+/* ------------------------------------------------------------------ */
+/* [P3 s3] lists backward among what its tutorial op leaves out; this is the
+ * gradient of y = gelu(x + bias) with the rounding points of an eager
+ * backward (gelu backward in the tensor dtype, then a column sum):
+ *     t          = round(x + bias[c])                   (as the forward)
+ *     grad_x     = round(grad_y * gelu'(t))
+ *     grad_bias  = round(sum over rows of grad_x[., c])  (exact sum)
+ * With s = sigma(2u) = 0.5 (1 + tanh(u)), u = sqrt(2/pi)(t + 0.044715 t^3):
+ *     gelu'(t) = s + t * 2 s (1 - s) * sqrt(2/pi) (1 + 3 * 0.044715 t^2),
+ * the derivative of t * s; s and 1 - s = sigma(-2u) are each evaluated on
+ * the side where they do not cancel. */
+static double sigmoid_exact(double z)
+{
+    if (z >= 0.0) return 1.0 / (1.0 + exp(-z));
+    const double e = exp(z);
+    return e / (1.0 + e);
+}
+
+static double gelu_tanh_grad(double t)
+{
+    const double k = sqrt(2.0 / acos(-1.0));
+    const double u = k * (t + 0.044715 * t * t * t);
+    const double s = sigmoid_exact(2.0 * u), one_minus_s = sigmoid_exact(-2.0 * u);
+    return s + t * 2.0 * s * one_minus_s * k * (1.0 + 3.0 * 0.044715 * t * t);
+}
+
+/* fmt: -1 = binary32, 0 = binary16, 1 = bfloat16.  Values travel as raw
+ * element bits (uint32 for binary32, uint16 otherwise).  gx64 / gb64, when
+ * given, receive the unrounded products and sums. */
+static double dec_any(const void *p, int64_t i, int fmt)
+{
+    if (fmt < 0) { float f; uint32_t b = ((const uint32_t *)p)[i]; memcpy(&f, &b, 4); return f; }
+    return dec16(((const uint16_t *)p)[i], fmt);
+}
+
+static void enc_any(void *p, int64_t i, double v, int fmt)
+{
+    if (fmt < 0) { float f = (float)v; uint32_t b; memcpy(&b, &f, 4); ((uint32_t *)p)[i] = b; }
+    else ((uint16_t *)p)[i] = enc16(v, fmt);
+}
+
+void orc_bias_gelu_bwd(const void *grad_y, const void *x, const void *bias, void *grad_x,
+                       void *grad_bias, double *gx64, double *gb64, int64_t rows, int32_t width,
+                       int fmt)
+{
+    double *sum = (double *)calloc((size_t)(width > 0 ? width : 1), sizeof(double));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t c = 0; c < width; ++c) {
+            int64_t i = r * (int64_t)width + c;
+            double t = dec_any(x, i, fmt) + dec_any(bias, c, fmt);
+            if (fmt < 0) t = (double)(float)t;   /* binary32 add: one rounding */
+            else t = dec16(enc16(t, fmt), fmt);
+            double g = dec_any(grad_y, i, fmt) * gelu_tanh_grad(t);
+            if (gx64) gx64[i] = g;
+            enc_any(grad_x, i, g, fmt);
+            sum[c] += dec_any(grad_x, i, fmt);     /* the rounded gradient, summed exactly */
+        }
+    for (int32_t c = 0; c < width; ++c) {
+        if (gb64) gb64[c] = sum[c];
+        enc_any(grad_bias, c, sum[c], fmt);
+    }
+    free(sum);
 }

@@ -546,3 +546,66 @@ def test_bf16_gelu():
     ref = torch.nn.functional.gelu(t, approximate="tanh").numpy()
     assert _close_to_torch(y64, t.numpy(), ref)
     assert np.array_equal(y, oracle.rnbf16(ref))
+
+
+# ------------------------------------------------------- GELU backward ----
+
+def test_gelu_backward_matches_torch_autograd_float64():
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(64, 96, generator=g, dtype=torch.float32)
+    b = torch.randn(96, generator=g, dtype=torch.float32) * 0.02
+    gy = torch.randn(64, 96, generator=g, dtype=torch.float32)
+    gx, gb, gx64, gb64 = oracle.bias_gelu_tanh_bwd(gy.numpy(), x.numpy(), b.numpy())
+    t = (x + b).double().requires_grad_(True)           # fp32 add, then exact
+    torch.nn.functional.gelu(t, approximate="tanh").backward(gy.double())
+    ref = t.grad.numpy()
+    assert np.all(np.abs(gx64 - ref) <= 1e-13 * np.abs(ref) + 1e-15 * np.abs(gy.numpy()))
+    assert np.array_equal(gx, ref.astype(np.float32))
+    assert np.allclose(gb64, gx.astype(np.float64).sum(axis=0), rtol=1e-14, atol=0)
+
+
+def _decimal_gelu_derivative(t: float) -> float:
+    """Central difference of the page's formula in 250-digit decimal
+    arithmetic with h = 1e-30 (truncation error ~1e-60)."""
+    import decimal
+    with decimal.localcontext() as ctx:
+        ctx.prec = 250
+        D = decimal.Decimal
+        pi = D("3.14159265358979323846264338327950288419716939937510582097494459230781640628620899")
+        k = (D(2) / pi).sqrt()
+
+        def f(v):
+            u = k * (v + D("0.044715") * v * v * v)
+            e2 = (2 * u).exp()
+            return D("0.5") * v * (1 + (e2 - 1) / (e2 + 1))
+
+        h = D("1e-30")
+        T = D(t)
+        return float((f(T + h) - f(T - h)) / (2 * h))
+
+
+def test_gelu_derivative_matches_high_precision_differences():
+    ts = np.array([-11.0, -9.5, -7.0, -4.5, -2.0, -0.5, 0.0, 0.3, 1.7, 6.0], dtype=np.float32)
+    one = np.ones((1, ts.size), np.float32)
+    _, _, d64, _ = oracle.bias_gelu_tanh_bwd(one, ts[None, :], np.zeros(ts.size, np.float32))
+    want = np.array([_decimal_gelu_derivative(float(t)) for t in ts])
+    assert np.all(np.abs(d64[0] - want) <= 1e-13 * np.abs(want) + 1e-300), (d64[0], want)
+
+
+def test_gelu_backward_16_bit_rounding_points():
+    g = torch.Generator().manual_seed(10)
+    for dt, fmt in ((torch.float16, "f16"), (torch.bfloat16, "bf16")):
+        x = torch.randn(48, 64, generator=g).to(dt)
+        b = (torch.randn(64, generator=g) * 0.02).to(dt)
+        gy = torch.randn(48, 64, generator=g).to(dt)
+        conv = (lambda a: a.numpy()) if fmt == "f16" else (lambda a: a.view(torch.int16).numpy().view(np.uint16))
+        gx, gb, gx64, gb64 = oracle.bias_gelu_tanh_bwd(conv(gy), conv(x), conv(b), fmt=fmt)
+        t = (x + b).double().requires_grad_(True)       # 16-bit add rounds t, then exact
+        torch.nn.functional.gelu(t, approximate="tanh").backward(gy.double())
+        ref = t.grad
+        assert np.allclose(gx64, ref.numpy(), rtol=1e-13, atol=1e-15)
+        want_gx = conv(ref.to(dt))
+        assert np.array_equal(gx, want_gx)
+        exact_sum = ref.to(dt).double().sum(0)         # sum of the rounded gradients
+        assert np.allclose(gb64, exact_sum.numpy(), rtol=1e-14, atol=1e-15)
+        assert np.array_equal(gb, conv(exact_sum.to(dt)))
