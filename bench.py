@@ -167,6 +167,19 @@ def build_next_calls():
         None, m))
     rows, width = synth.GELU_F16_SHAPE
     xg, bg = synth.gelu_input(rows, width, bf, seed=4)
+    # backward of bias + GELU (algorithmic bytes: grad_y and x read, grad_x
+    # written, bias read and grad_bias written; the partial sums are extra)
+    for (r_, w_), dt_ in ((synth.GELU_F32_SHAPE, torch.float32), (synth.GELU_F16_SHAPE, torch.float16)):
+        esz = 4 if dt_ == torch.float32 else 2
+        xg_, bg_ = synth.gelu_input(r_, w_, dt_, seed=4)
+        gy_, _ = synth.gelu_input(r_, w_, dt_, seed=5)
+        calls.append(Call(
+            "bias_gelu_tanh_bwd", f"{'fp32' if esz == 4 else 'fp16'} [{r_},{w_}]",
+            3 * r_ * w_ * esz + 2 * w_ * esz, {"gy": gy_, "x": xg_, "bias": bg_},
+            {"gx": ((r_, w_), dt_), "gb": ((w_,), dt_), "ws": ((wgs.gelu_bwd_workspace_bytes(r_, w_),), torch.uint8)},
+            lambda i, o: wgs.bias_gelu_tanh_bwd(i["gy"], i["x"], i["bias"], grad_x=o["gx"],
+                                                grad_bias=o["gb"], workspace=o["ws"]),
+            None, r_))
     calls.append(Call("bias_gelu_tanh", f"bf16 [{rows},{width}]", 4 * rows * width + 2 * width,
                       {"x": xg, "bias": bg}, {"y": ((rows, width), bf)},
                       lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]), None, rows))

@@ -225,6 +225,34 @@ wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows
                           wgs_dtype dtype, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* bias_gelu_tanh_bwd -- backward of bias + tanh-GELU                   */
+/*          [P3 s3: the tutorial op leaves backward out; this adds it]  */
+/* ------------------------------------------------------------------ */
+/* Gradient of y = gelu_tanh(x + bias) with an eager backward's rounding
+ * points:
+ *     t         = round(x + bias[c])                         (as forward)
+ *     grad_x    = round(grad_y * gelu'(t))   (gelu' evaluated in FP32)
+ *     grad_bias = round(sum over rows of grad_x[., c])       (FP32 sum)
+ * The column sum is deterministic: per-slab FP32 partial sums go to
+ * `workspace`, then one pass adds them in a fixed order; the slab count
+ * depends only on `rows`, so results do not depend on the device.
+ *   grad_y, x, grad_x  [rows, width] of `dtype`; grad_x may equal grad_y,
+ *          other overlaps return WGS_ERR_ALIAS.
+ *   bias, grad_bias    [width] of `dtype`, disjoint from everything else.
+ *   workspace  device memory of at least
+ *          wgs_bias_gelu_bwd_workspace_bytes(rows, width) bytes, 16-byte
+ *          aligned, owned by the caller, disjoint from the tensors; its
+ *          contents on entry do not matter.
+ *   rows == 0 writes grad_bias = 0 (one small launch); width == 0 returns
+ *   WGS_OK and launches nothing.  The 16-byte vector path needs width a
+ *   multiple of 4 (f32) or 8 (16-bit types) and aligned tensors; otherwise
+ *   a scalar path runs (same results). */
+size_t wgs_bias_gelu_bwd_workspace_bytes(int64_t rows, int32_t width);
+wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bias, void *grad_x,
+                              void *grad_bias, void *workspace, size_t workspace_bytes,
+                              int64_t rows, int32_t width, wgs_dtype dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* Host-side window index map                                 [P1 s5] */
 /* ------------------------------------------------------------------ */
 /* The page fixes the protocol (INT32 per destination row, >= 0 source

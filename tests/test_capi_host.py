@@ -220,3 +220,23 @@ def test_block_boundary_argument_errors(lib):
     assert ang(A, B, C + 1, D, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIGN
     assert ang(A, B, C, D, D + 128, 10, 12, 192, 1e-5, None) == ALIAS    # dst inside r
     assert ang(A, B, C, A + 768, A + 2 ** 20, 10, 12, 192, 1e-5, None) == ALIAS  # shifted r
+
+
+def test_gelu_backward_argument_errors(lib):
+    f = lib.bias_gelu_tanh_bwd
+    need = lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 768)
+    assert need == 16 * 768 * 4                      # 1000 rows -> 16 slabs of >= 64 rows
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(131040, 768) == 512 * 768 * 4
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(0, 768) == 0
+    W = 0x50000000
+    assert f(A, B, C, D, A + 2 ** 24, W, need, 1000, 768, 5, None) == DTYPE
+    assert f(A, B, C, D, A + 2 ** 24, W, need, -1, 768, 0, None) == SHAPE
+    assert f(None, None, None, None, None, None, 0, 1000, 0, 0, None) == OK   # width 0
+    assert f(A, B, None, D, A + 2 ** 24, W, need, 1000, 768, 0, None) == NULL
+    assert f(A, B, C, D, A + 2 ** 24, None, need, 1000, 768, 0, None) == NULL
+    assert f(A, B, C, D, A + 2 ** 24, W, need - 4, 1000, 768, 0, None) == SHAPE
+    assert f(A, B, C, D, A + 2 ** 24, W + 4, need, 1000, 768, 0, None) == ALIGN
+    assert f(A + 2, B, C, D, A + 2 ** 24, W, need, 1000, 768, 0, None) == ALIGN
+    assert f(A, B, C, B + 64, A + 2 ** 24, W, need, 1000, 768, 0, None) == ALIAS   # grad_x in x
+    assert f(A, B, C, D, C + 4, W, need, 1000, 768, 0, None) == ALIAS             # grad_bias in bias
+    assert f(A, B, C, D, A + 2 ** 24, D + 64, need, 1000, 768, 0, None) == ALIAS  # workspace in grad_x

@@ -532,6 +532,97 @@ def test_bf16_gelu(rows, width):
     print("gelu bf16", check_bf16_near(_bits(y), o, y64, f"gelu bf16 {rows}x{width}"))
 
 
+# ------------------------------------------------------- GELU backward ----
+
+def _values(a, fmt):
+    if fmt == "f32":
+        return a.astype(np.float64)
+    if fmt == "f16":
+        return a.astype(np.float64)
+    from parity import bf16_values
+    return bf16_values(a)
+
+
+def _spacing(v, fmt):
+    from parity import bf16_spacing, fp16_spacing
+    if fmt == "f32":
+        a = np.abs(v)
+        return np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 23.0)
+    return fp16_spacing(v) if fmt == "f16" else bf16_spacing(v)
+
+
+def _check_bwd(gy, x, b, gx, gb, fmt, what):
+    """grad_x against the oracle within the FP32 error bound; grad_bias
+    against the exact sum of the GPU's own rounded grad_x within the bound
+    of a recursive FP32 sum (at most ~1024 additions deep)."""
+    o_gx, o_gb, gx64, gb64 = oracle.bias_gelu_tanh_bwd(gy, x, b, fmt=fmt)
+    gxv = _values(gx, fmt)
+    gyv = _values(gy, fmt)
+    err = np.abs(gxv - gx64)
+    bound = 0.5 * _spacing(gxv, fmt) + 1e-5 * np.abs(gx64) + 1e-6 * np.abs(gyv) + 1e-38
+    fin = np.isfinite(gx64)
+    assert np.array_equal(np.isnan(gxv), np.isnan(gx64)), what
+    bad = (err > bound) & fin
+    assert not bad.any(), (what, int(bad.sum()), gxv[bad][:4], gx64[bad][:4])
+    own = gxv.sum(axis=0)
+    depth_bound = 1024 * 2.0 ** -24 * np.abs(gxv).sum(axis=0)
+    gbv = _values(gb, fmt)
+    lim = depth_bound + 0.5 * _spacing(gbv, fmt) + 1e-30
+    assert np.all(np.abs(gbv - own) <= lim), (what, np.max(np.abs(gbv - own) / lim))
+    return {"max_gx_err_over_bound": float((err[fin] / bound[fin]).max(initial=0)),
+            "max_gb_err_over_bound": float((np.abs(gbv - own) / lim).max(initial=0))}
+
+
+def _bwd_inputs(rows, width, dtype, seed):
+    x, b = synth.gelu_input(rows, width, dtype, seed=seed)
+    gy, _ = synth.gelu_input(rows, width, dtype, seed=seed + 1)
+    return gy, x, b
+
+
+def _np_of(t, fmt):
+    return _bits(t) if fmt == "bf16" else t.numpy()
+
+
+@pytest.mark.parametrize("dtype,fmt", [(torch.float32, "f32"), (torch.float16, "f16"),
+                                       (torch.bfloat16, "bf16")])
+@pytest.mark.parametrize("rows,width", [(131040, 768), (32760, 1536), (1, 768), (63, 8),
+                                        (1000, 1000), (7, 3), (4097, 4104)])
+def test_gelu_backward(rows, width, dtype, fmt):
+    if rows * width > 40_000_000 and dtype != torch.float32 and width != 1536:
+        pytest.skip("one large 16-bit case is enough")
+    gy, x, b = _bwd_inputs(rows, width, dtype, seed=rows + width)
+    gx, gb = wgs.bias_gelu_tanh_bwd(gy.to(DEV), x.to(DEV), b.to(DEV))
+    st = _check_bwd(_np_of(gy, fmt), _np_of(x, fmt), _np_of(b, fmt), _np_of(gx.cpu(), fmt),
+                    _np_of(gb.cpu(), fmt), fmt, f"gelu bwd {fmt} {rows}x{width}")
+    print("gelu bwd", fmt, rows, width, st)
+
+
+def test_gelu_backward_edges():
+    # no rows: grad_bias is zero; misaligned views take the scalar path
+    b = torch.randn(768, device=DEV)
+    gx, gb = wgs.bias_gelu_tanh_bwd(torch.empty(0, 768, device=DEV), torch.empty(0, 768, device=DEV), b)
+    assert gx.shape == (0, 768) and (gb == 0).all()
+    gy, x, bb = _bwd_inputs(65, 769, torch.float32, seed=3)
+    xd = x.to(DEV).view(-1)[1:1 + 64 * 768].view(64, 768)
+    gyd = gy.to(DEV).view(-1)[1:1 + 64 * 768].view(64, 768)
+    gx, gb = wgs.bias_gelu_tanh_bwd(gyd, xd, bb.to(DEV)[1:])
+    _check_bwd(np_(gyd), np_(xd), np_(bb.to(DEV)[1:]), np_(gx), np_(gb), "f32", "bwd misaligned")
+    # deterministic: two calls give the same bits; in place over grad_y matches
+    gy, x, bb = _bwd_inputs(5000, 768, torch.float32, seed=4)
+    gy, x, bb = gy.to(DEV), x.to(DEV), bb.to(DEV)
+    g1 = wgs.bias_gelu_tanh_bwd(gy, x, bb)
+    g2 = wgs.bias_gelu_tanh_bwd(gy, x, bb)
+    assert torch.equal(g1[0], g2[0]) and torch.equal(g1[1], g2[1])
+    gy2 = gy.clone()
+    g3 = wgs.bias_gelu_tanh_bwd(gy2, x, bb, grad_x=gy2)
+    assert torch.equal(gy2, g1[0]) and torch.equal(g3[1], g1[1])
+    # far-left and special inputs
+    t = torch.tensor([[-11.0, -7.5, -4.5, -3.9, -0.7518, 0.0, 2.0, 30.0]], device=DEV)
+    z = torch.zeros(8, device=DEV)
+    gx, gb = wgs.bias_gelu_tanh_bwd(torch.ones_like(t), t, z)
+    _check_bwd(np.ones((1, 8), np.float32), np_(t), np_(z), np_(gx), np_(gb), "f32", "bwd specials")
+
+
 # ------------------------------------------------------- graph capture ----
 
 def test_identical_results_when_captured_in_a_cuda_graph():

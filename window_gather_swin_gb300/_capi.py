@@ -39,6 +39,8 @@ SIGNATURES = {
     "norm_gather_bf16": (_st, [_P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "window_reverse_add_ln_fwd_bf16": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "residual_add_norm_gather_bf16": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
+    "wgs_bias_gelu_bwd_workspace_bytes": (ctypes.c_size_t, [_i64, _i32]),
+    "bias_gelu_tanh_bwd": (_st, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _i64, _i32, _i32, _P]),
     "wgs_window_index_count": (_i64, [_P, _P, _P]),
     "wgs_build_window_index": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
     "wgs_check_error": (_st, [_P]),

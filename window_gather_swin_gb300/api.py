@@ -215,6 +215,43 @@ def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
     return y
 
 
+def gelu_bwd_workspace_bytes(rows: int, width: int) -> int:
+    """Bytes of workspace bias_gelu_tanh_bwd needs for a [rows, width] tensor."""
+    return int(_capi.load().wgs_bias_gelu_bwd_workspace_bytes(max(int(rows), 1), int(width)))
+
+
+def bias_gelu_tanh_bwd(grad_y: torch.Tensor, x: torch.Tensor, bias: torch.Tensor,
+                       grad_x: Optional[torch.Tensor] = None,
+                       grad_bias: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None):
+    """Backward of gelu_tanh(x + bias).  Returns (grad_x, grad_bias).  The
+    deterministic column sum needs a workspace of
+    wgs_bias_gelu_bwd_workspace_bytes(rows, width) bytes; one is allocated
+    here unless the caller passes a uint8 CUDA tensor that large."""
+    _cuda(x, "x")
+    _require(x.dtype in _DTYPE, f"x must be float32, float16 or bfloat16 (got {x.dtype})")
+    _cuda(grad_y, "grad_y", x.dtype)
+    _cuda(bias, "bias", x.dtype)
+    _require(grad_y.shape == x.shape and x.dim() >= 1, "grad_y and x must have the same shape")
+    width = x.shape[-1]
+    _require(bias.dim() == 1 and bias.numel() == width,
+             f"bias must be 1-D with {width} elements (got shape {tuple(bias.shape)})")
+    rows = x.numel() // width if width else 0
+    gx = _out(grad_x, x.shape, x.dtype, x.device, "grad_x")
+    gb = _out(grad_bias, bias.shape, x.dtype, x.device, "grad_bias")
+    lib = _capi.load()
+    need = int(lib.wgs_bias_gelu_bwd_workspace_bytes(max(rows, 1), width))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _cuda(workspace, "workspace", torch.uint8)
+    _same_device(grad_y, x, bias, gx, gb, workspace)
+    with torch.cuda.device(x.device):
+        _capi.check("bias_gelu_tanh_bwd", lib.bias_gelu_tanh_bwd(
+            _ptr(grad_y), _ptr(x), _ptr(bias), _ptr(gx), _ptr(gb), _ptr(workspace),
+            workspace.numel(), rows, width, _DTYPE[x.dtype], _stream_ptr(x.device)))
+    return gx, gb
+
+
 # ----------------------------------------------------------- index map ----
 
 SHIFT_THEN_PAD, PAD_THEN_SHIFT = 0, 1

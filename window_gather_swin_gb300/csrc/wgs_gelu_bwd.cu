@@ -1,0 +1,344 @@
+// Backward of the fused bias + tanh-GELU epilogue (sm_103a).
+//
+// Page "PyTorch + HIP fused bias + GELU on Hygon DCU", s3, leaves backward
+// out of its tutorial op; this is the gradient of y = gelu(x + bias) with
+// the rounding points of an eager backward:
+//     t         = round(x + bias[c])                     (as the forward)
+//     grad_x    = round(grad_y * gelu'(t))
+//     grad_bias = round(sum over rows of grad_x[., c])
+// With s = 1 / (1 + 2^w), w = t (c1 + c3 t^2) as in the forward (so
+// s = 0.5 (1 + tanh u)) and 1 - s = 2^w s:
+//     gelu'(t) = s + t s (1 - s) (2k + 6k a t^2),   k = sqrt(2/pi), a = 0.044715.
+// Below t = -4 the FP64 form runs, as in the forward.
+//
+// The column sum is deterministic and runs in two passes:
+//   1. grid (slab, column block): every thread owns one 16-byte column chunk
+//      (or one column on the scalar path), walks rows r0 + g, r0 + g + G, ...
+//      of its slab, stores grad_x and accumulates the rounded gradients in
+//      FP32 registers; the G row groups of the CTA then combine in shared
+//      memory in a fixed order into partial[slab][column];
+//   2. one thread per column sums partial[0..slabs) in order.
+// The slab count depends only on the row count, so results do not depend
+// on the device.  Both passes stream: grad_y and x are read once and grad_x
+// is written once; the partials are a few MB at most.
+#include <atomic>
+#include <type_traits>
+
+#include "wgs_common.cuh"
+
+namespace wgs {
+
+namespace {
+
+struct F32 {};
+
+constexpr double kSqrt2OverPi = 0.7978845608028654;
+constexpr double kLog2e = 1.4426950408889634;
+constexpr float kFarLeft = -4.0f;
+constexpr int64_t kMinRowsPerSlab = 64;
+constexpr int64_t kMaxSlabs = 512;
+constexpr int kMaxChunksPerBlock = 256;  // column chunks per CTA
+constexpr int kMaxThreads = 512;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __noinline__ float gelu_grad_far_left(float t) {
+    const double td = t;
+    const double k = kSqrt2OverPi;
+    const double z = td * (-2.0 * k) * (1.0 + 0.044715 * td * td);  // -2u
+    const double e = exp(z);                 // e^{-2u}, may be +inf
+    const double s = 1.0 / (1.0 + e);        // 0.5 (1 + tanh u)
+    const double one_minus_s = 1.0 / (1.0 + 1.0 / e);
+    return static_cast<float>(s + td * s * one_minus_s * (2.0 * k) * (1.0 + 3.0 * 0.044715 * td * td));
+}
+
+__device__ __forceinline__ float gelu_grad(float t) {
+    constexpr float c1 = static_cast<float>(-2.0 * kSqrt2OverPi * kLog2e);
+    constexpr float c3 = static_cast<float>(-2.0 * kSqrt2OverPi * 0.044715 * kLog2e);
+    constexpr float k1 = static_cast<float>(2.0 * kSqrt2OverPi);
+    constexpr float k3 = static_cast<float>(6.0 * kSqrt2OverPi * 0.044715);
+    if (t < kFarLeft) return gelu_grad_far_left(t);
+    const float t2 = t * t;
+    const float e = ex2_approx(t * fmaf(c3, t2, c1));
+    const float s = rcp_approx(1.0f + e);
+    return fmaf(t * s * (e * s), fmaf(k3, t2, k1), s);
+}
+
+// Gradient of the two 16-bit elements of one word: returns the rounded
+// grad_x word and adds the rounded values to acc[0..1].
+template <typename E>
+__device__ __forceinline__ uint32_t grad_word16(uint32_t gy, uint32_t x, uint32_t b, float *acc) {
+    const float2 t = E::to_f2(E::add2(x, b));
+    const float2 g = E::to_f2(gy);
+    const uint32_t r = E::from_f2(g.x * gelu_grad(t.x), g.y * gelu_grad(t.y));
+    const float2 rv = E::to_f2(r);
+    acc[0] += rv.x;
+    acc[1] += rv.y;
+    return r;
+}
+
+// Pass 1, 16-byte chunks.  Block = CVB * G threads: thread (g, j) owns
+// column chunk blockIdx.y * CVB + j and walks every G-th row of the slab.
+template <typename E>
+__global__ void __launch_bounds__(kMaxThreads)
+gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
+                int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
+                int32_t slabs) {
+    pdl_prologue();
+    constexpr bool k16 = !std::is_same<E, F32>::value;
+    constexpr int kN = k16 ? 8 : 4;
+    extern __shared__ float red[];  // [groups][cvb][kN]
+    const int j = threadIdx.x % cvb, g = threadIdx.x / cvb;
+    const int32_t cv = static_cast<int32_t>(blockIdx.y) * cvb + j;
+    const bool active = g < groups && cv < row_chunks;
+    const int64_t r0 = rows * blockIdx.x / slabs, r1 = rows * (blockIdx.x + 1) / slabs;
+    float acc[kN];
+#pragma unroll
+    for (int e = 0; e < kN; ++e) acc[e] = 0.f;
+    if (active) {
+        const uint4 bv = __ldg(bias + cv);
+        int64_t r = r0 + g;
+        // two rows in flight per iteration
+        for (; r + groups < r1; r += 2 * groups) {
+            const int64_t i0 = r * row_chunks + cv, i1 = (r + groups) * row_chunks + cv;
+            const uint4 gy0 = ld_stream(gy + i0), x0 = ld_stream(x + i0);
+            const uint4 gy1 = ld_stream(gy + i1), x1 = ld_stream(x + i1);
+            uint4 o0, o1;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if constexpr (k16) {
+                    set_word(o0, w, grad_word16<E>(word(gy0, w), word(x0, w), word(bv, w), acc + 2 * w));
+                } else {
+                    const float t = __uint_as_float(word(x0, w)) + __uint_as_float(word(bv, w));
+                    const float v = __uint_as_float(word(gy0, w)) * gelu_grad(t);
+                    acc[w] += v;
+                    set_word(o0, w, __float_as_uint(v));
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if constexpr (k16) {
+                    set_word(o1, w, grad_word16<E>(word(gy1, w), word(x1, w), word(bv, w), acc + 2 * w));
+                } else {
+                    const float t = __uint_as_float(word(x1, w)) + __uint_as_float(word(bv, w));
+                    const float v = __uint_as_float(word(gy1, w)) * gelu_grad(t);
+                    acc[w] += v;
+                    set_word(o1, w, __float_as_uint(v));
+                }
+            }
+            st_stream(gx + i0, o0);
+            st_stream(gx + i1, o1);
+        }
+        if (r < r1) {
+            const int64_t i0 = r * row_chunks + cv;
+            const uint4 gy0 = ld_stream(gy + i0), x0 = ld_stream(x + i0);
+            uint4 o0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if constexpr (k16) {
+                    set_word(o0, w, grad_word16<E>(word(gy0, w), word(x0, w), word(bv, w), acc + 2 * w));
+                } else {
+                    const float t = __uint_as_float(word(x0, w)) + __uint_as_float(word(bv, w));
+                    const float v = __uint_as_float(word(gy0, w)) * gelu_grad(t);
+                    acc[w] += v;
+                    set_word(o0, w, __float_as_uint(v));
+                }
+            }
+            st_stream(gx + i0, o0);
+        }
+    }
+    // combine the row groups in a fixed order
+    if (g < groups)
+#pragma unroll
+        for (int e = 0; e < kN; ++e) red[(g * cvb + j) * kN + e] = acc[e];
+    __syncthreads();
+    if (g == 0 && cv < row_chunks) {
+#pragma unroll
+        for (int e = 0; e < kN; ++e) {
+            float s = red[j * kN + e];
+            for (int q = 1; q < groups; ++q) s += red[(q * cvb + j) * kN + e];
+            partial[static_cast<int64_t>(blockIdx.x) * width + cv * kN + e] = s;
+        }
+    }
+}
+
+// Pass 1, any width / alignment: thread (g, j) owns column blockIdx.y*CVB + j.
+template <typename E>
+__global__ void __launch_bounds__(kMaxThreads)
+gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, float *partial,
+                int64_t rows, int32_t width, int32_t cvb, int32_t groups, int32_t slabs) {
+    pdl_prologue();
+    constexpr bool k16 = !std::is_same<E, F32>::value;
+    extern __shared__ float red[];  // [groups][cvb]
+    const int j = threadIdx.x % cvb, g = threadIdx.x / cvb;
+    const int32_t c = static_cast<int32_t>(blockIdx.y) * cvb + j;
+    const bool active = g < groups && c < width;
+    const int64_t r0 = rows * blockIdx.x / slabs, r1 = rows * (blockIdx.x + 1) / slabs;
+    float acc = 0.f;
+    if (active) {
+        for (int64_t r = r0 + g; r < r1; r += groups) {
+            const int64_t i = r * width + c;
+            if constexpr (k16) {
+                const uint16_t *gy = static_cast<const uint16_t *>(gyp);
+                const uint16_t *x = static_cast<const uint16_t *>(xp);
+                const uint16_t *b = static_cast<const uint16_t *>(bp);
+                const float t = E::to_f2(E::add2(x[i], b[c])).x;
+                const uint16_t o = static_cast<uint16_t>(E::from_f2(E::to_f2(gy[i]).x * gelu_grad(t), 0.f));
+                static_cast<uint16_t *>(gxp)[i] = o;
+                acc += E::to_f2(o).x;
+            } else {
+                const float *gy = static_cast<const float *>(gyp);
+                const float *x = static_cast<const float *>(xp);
+                const float *b = static_cast<const float *>(bp);
+                const float v = gy[i] * gelu_grad(x[i] + b[c]);
+                static_cast<float *>(gxp)[i] = v;
+                acc += v;
+            }
+        }
+    }
+    if (g < groups) red[g * cvb + j] = acc;
+    __syncthreads();
+    if (g == 0 && c < width) {
+        float s = red[j];
+        for (int q = 1; q < groups; ++q) s += red[q * cvb + j];
+        partial[static_cast<int64_t>(blockIdx.x) * width + c] = s;
+    }
+}
+
+// Pass 2: grad_bias[c] = round(sum over slabs of partial[slab][c]), in slab order.
+template <typename E>
+__global__ void __launch_bounds__(256)
+gelu_bwd_bias(const float *partial, void *grad_bias, int32_t width, int32_t slabs) {
+    pdl_prologue();
+    const int32_t c = static_cast<int32_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= width) return;
+    float s = 0.f;
+    for (int32_t q = 0; q < slabs; ++q) s += partial[static_cast<int64_t>(q) * width + c];
+    if constexpr (std::is_same<E, F32>::value)
+        static_cast<float *>(grad_bias)[c] = s;
+    else
+        static_cast<uint16_t *>(grad_bias)[c] = static_cast<uint16_t>(E::from_f2(s, 0.f));
+}
+
+int64_t slabs_for(int64_t rows) {
+    int64_t s = ceil_div(rows, kMinRowsPerSlab);
+    return s < 1 ? 1 : (s > kMaxSlabs ? kMaxSlabs : s);
+}
+
+template <typename E>
+wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx, void *gb,
+                      float *partial, int64_t rows, int32_t width, cudaStream_t stream) {
+    constexpr bool k16 = !std::is_same<E, F32>::value;
+    constexpr int kVec = k16 ? 8 : 4;
+    const int32_t slabs = static_cast<int32_t>(slabs_for(rows));
+    const bool chunks = width % kVec == 0 && aligned16(gy) && aligned16(x) && aligned16(bias) &&
+                        aligned16(gx);
+    const int32_t units = chunks ? width / kVec : width;        // column units per row
+    const int32_t cvb = units < kMaxChunksPerBlock ? units : kMaxChunksPerBlock;
+    int32_t groups = kMaxThreads / cvb;
+    if (groups > 8) groups = 8;
+    if (groups < 1) groups = 1;
+    const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ceil_div(units, cvb)));
+    const dim3 block(static_cast<unsigned>(cvb * groups));
+    wgs_status st;
+    if (chunks) {
+        const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
+        st = launch(gelu_bwd_chunks<E>, grid, block, smem, stream, static_cast<const uint4 *>(gy),
+                    static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
+                    static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups, slabs);
+    } else {
+        const size_t smem = static_cast<size_t>(groups) * cvb * sizeof(float);
+        st = launch(gelu_bwd_scalar<E>, grid, block, smem, stream, gy, x, bias, gx, partial, rows,
+                    width, cvb, groups, slabs);
+    }
+    if (st != WGS_OK) return st;
+    return launch(gelu_bwd_bias<E>, dim3(static_cast<unsigned>(ceil_div(width, 256))), dim3(256), 0,
+                  stream, static_cast<const float *>(partial), gb, width, slabs);
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int64_t rows, int32_t width) {
+    if (rows <= 0 || width <= 0) return 0;
+    return static_cast<size_t>(slabs_for(rows)) * static_cast<size_t>(width) * sizeof(float);
+}
+
+wgs_status bias_gelu_bwd_checked(const void *grad_y, const void *x, const void *bias,
+                                 void *grad_x, void *grad_bias, float *partial, int64_t rows,
+                                 int32_t width, wgs_dtype dtype, cudaStream_t stream) {
+    DeviceInfo dev;
+    const wgs_status st = current_device(&dev);
+    if (st != WGS_OK) return st;
+    switch (dtype) {
+        case WGS_F16:
+            return launch_bwd<Fp16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+        case WGS_BF16:
+            return launch_bwd<Bf16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+        default:
+            return launch_bwd<F32>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+    }
+}
+
+// Argument checks shared by the entry points.
+wgs_status bias_gelu_bwd_args(const void *grad_y, const void *x, const void *bias, void *grad_x,
+                              void *grad_bias, int64_t rows, int32_t width, wgs_dtype dtype) {
+    if (dtype != WGS_F32 && dtype != WGS_F16 && dtype != WGS_BF16) return WGS_ERR_DTYPE;
+    if (rows < 0 || width < 0) return WGS_ERR_SHAPE;
+    const int64_t esz = dtype == WGS_F32 ? 4 : 2;
+    if (width > 0 && rows > INT64_MAX / esz / width) return WGS_ERR_SHAPE;
+    if (width == 0) return WGS_OK;
+    if (!bias || !grad_bias) return WGS_ERR_NULL;
+    if (rows > 0 && (!grad_y || !x || !grad_x)) return WGS_ERR_NULL;
+    const uintptr_t mask = static_cast<uintptr_t>(esz - 1);
+    if ((reinterpret_cast<uintptr_t>(grad_y) | reinterpret_cast<uintptr_t>(x) |
+         reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(grad_x) |
+         reinterpret_cast<uintptr_t>(grad_bias)) & mask)
+        return WGS_ERR_ALIGN;
+    const int64_t bytes = rows * width * esz, bbytes = width * esz;
+    if (!same_or_disjoint(grad_x, grad_y, bytes) || overlap(grad_x, bytes, x, bytes) ||
+        overlap(grad_x, bytes, bias, bbytes) || overlap(grad_bias, bbytes, grad_y, bytes) ||
+        overlap(grad_bias, bbytes, x, bytes) || overlap(grad_bias, bbytes, grad_x, bytes) ||
+        overlap(grad_bias, bbytes, bias, bbytes))
+        return WGS_ERR_ALIAS;
+    return WGS_OK;
+}
+
+}  // namespace wgs
+
+using namespace wgs;
+
+extern "C" size_t wgs_bias_gelu_bwd_workspace_bytes(int64_t rows, int32_t width) {
+    return bwd_workspace_bytes(rows, width);
+}
+
+extern "C" wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bias,
+                                         void *grad_x, void *grad_bias, void *workspace,
+                                         size_t workspace_bytes, int64_t rows, int32_t width,
+                                         wgs_dtype dtype, cudaStream_t stream) {
+    wgs_status st = bias_gelu_bwd_args(grad_y, x, bias, grad_x, grad_bias, rows, width, dtype);
+    if (st != WGS_OK || width == 0) return st;
+    const size_t need = bwd_workspace_bytes(rows > 0 ? rows : 1, width);
+    if (!workspace) return WGS_ERR_NULL;
+    if (workspace_bytes < need) return WGS_ERR_SHAPE;
+    if (!aligned16(workspace)) return WGS_ERR_ALIGN;
+    const int64_t esz = dtype == WGS_F32 ? 4 : 2;
+    const int64_t bytes = rows * width * esz;
+    if (overlap(workspace, static_cast<int64_t>(need), grad_y, bytes) ||
+        overlap(workspace, static_cast<int64_t>(need), x, bytes) ||
+        overlap(workspace, static_cast<int64_t>(need), grad_x, bytes) ||
+        overlap(workspace, static_cast<int64_t>(need), bias, width * esz) ||
+        overlap(workspace, static_cast<int64_t>(need), grad_bias, width * esz))
+        return WGS_ERR_ALIAS;
+    return bias_gelu_bwd_checked(grad_y, x, bias, grad_x, grad_bias, static_cast<float *>(workspace),
+                                 rows, width, dtype, stream);
+}
