@@ -57,7 +57,8 @@ typedef enum {
     WGS_ERR_LAUNCH = 7,  /* the CUDA runtime rejected the launch            */
     WGS_ERR_INDEX = 8,   /* a gather index was outside [-1, n_src)          */
     WGS_ERR_ALIAS = 9,   /* buffers overlap in a way the operation forbids  */
-    WGS_ERR_CUDA = 10    /* another CUDA runtime call failed                */
+    WGS_ERR_CUDA = 10,   /* another CUDA runtime call failed                */
+    WGS_ERR_TOO_LARGE = 11 /* larger than the library's fixed scratch       */
 } wgs_status;
 
 typedef enum { WGS_F32 = 0, WGS_F16 = 1, WGS_BF16 = 2 } wgs_dtype;
@@ -251,6 +252,30 @@ size_t wgs_bias_gelu_bwd_workspace_bytes(int64_t rows, int32_t width);
 wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bias, void *grad_x,
                               void *grad_bias, void *workspace, size_t workspace_bytes,
                               int64_t rows, int32_t width, wgs_dtype dtype, cudaStream_t stream);
+
+/* bias_gelu_tanh_bwd_noalloc -- the same backward without a workspace.
+ * The reference pages have no counterpart; it exists for callers that
+ * cannot give this library device memory: an op inside a host runtime that
+ * owns every allocation and passes its plugins no allocator or workspace,
+ * or a hot path that must not call cudaMalloc because that call can
+ * synchronise the device.  The partial column sums then live in one array
+ * of 1,048,576 floats (4 MiB) built into the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *   Arguments, results and errors as bias_gelu_tanh_bwd, without
+ *   `workspace`.  Sizes whose partial sums would not fit (more than
+ *   1,048,576 floats: min(512, ceil(rows / 64)) slabs x width, so any row
+ *   count up to width 2048) return WGS_ERR_TOO_LARGE and launch nothing.
+ *   Allocates nothing.  The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress, with that device current); make
+ *   that first call before any stream capture.
+ *   All calls on a device share the array, which keeps whatever the last
+ *   call left there; nothing in it needs to start at zero, because every
+ *   partial sum is written before it is read.  Calls whose work overlaps on
+ *   the GPU (other streams, other host threads) race on the array: run one
+ *   at a time per device. */
+wgs_status bias_gelu_tanh_bwd_noalloc(const void *grad_y, const void *x, const void *bias,
+                                      void *grad_x, void *grad_bias, int64_t rows, int32_t width,
+                                      wgs_dtype dtype, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Host-side window index map                                 [P1 s5] */

@@ -14,7 +14,7 @@ from . import build as _build
 STATUS_NAMES = {
     0: "WGS_OK", 1: "WGS_ERR_NULL", 2: "WGS_ERR_SHAPE", 3: "WGS_ERR_WIDTH",
     4: "WGS_ERR_ALIGN", 5: "WGS_ERR_DTYPE", 6: "WGS_ERR_ARCH", 7: "WGS_ERR_LAUNCH",
-    8: "WGS_ERR_INDEX", 9: "WGS_ERR_ALIAS", 10: "WGS_ERR_CUDA",
+    8: "WGS_ERR_INDEX", 9: "WGS_ERR_ALIAS", 10: "WGS_ERR_CUDA", 11: "WGS_ERR_TOO_LARGE",
 }
 WGS_F32, WGS_F16, WGS_BF16 = 0, 1, 2
 
@@ -41,6 +41,7 @@ SIGNATURES = {
     "residual_add_norm_gather_bf16": (_st, [_P, _P, _P, _P, _P, _i64, _i64, _i32, _f32, _P]),
     "wgs_bias_gelu_bwd_workspace_bytes": (ctypes.c_size_t, [_i64, _i32]),
     "bias_gelu_tanh_bwd": (_st, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _i64, _i32, _i32, _P]),
+    "bias_gelu_tanh_bwd_noalloc": (_st, [_P, _P, _P, _P, _P, _i64, _i32, _i32, _P]),
     "wgs_window_index_count": (_i64, [_P, _P, _P]),
     "wgs_build_window_index": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
     "wgs_check_error": (_st, [_P]),

@@ -22,6 +22,7 @@
 // on the device.  Both passes stream: grad_y and x are read once and grad_x
 // is written once; the partials are a few MB at most.
 #include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "wgs_common.cuh"
@@ -341,4 +342,64 @@ extern "C" wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, cons
         return WGS_ERR_ALIAS;
     return bias_gelu_bwd_checked(grad_y, x, bias, grad_x, grad_bias, static_cast<float *>(workspace),
                                  rows, width, dtype, stream);
+}
+
+// ---------------------------------------------------------------------
+// The same backward without a caller workspace.
+//
+// Some callers cannot hand this library device memory: an op embedded in a
+// host runtime that owns every allocation and offers its plugins neither an
+// allocator nor a workspace argument, or a hot path that must not call
+// cudaMalloc because that call can synchronise the whole device.  For
+// them the partial column sums live in a fixed array compiled into the
+// library.  Every GPU that loads the library holds the array until the
+// process exits, and all calls on that GPU share it.
+// ---------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = size_t{1} << 20;  // 4 MiB per device
+
+static __device__ __align__(256) float g_bwd_scratch[kNoAllocScratchFloats];
+
+// Host code cannot use g_bwd_scratch as a pointer (on the host it names a
+// stand-in object, not device memory), so each device's address is looked
+// up once, with that device current, and kept here.
+std::mutex g_scratch_mutex;
+float *g_scratch_ptr[64] = {};
+
+wgs_status scratch_for(int device, float **out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();  // clear this thread's error
+            return WGS_ERR_CUDA;
+        }
+        g_scratch_ptr[device] = static_cast<float *>(p);
+    }
+    *out = g_scratch_ptr[device];
+    return WGS_OK;
+}
+
+}  // namespace
+
+extern "C" wgs_status bias_gelu_tanh_bwd_noalloc(const void *grad_y, const void *x,
+                                                 const void *bias, void *grad_x, void *grad_bias,
+                                                 int64_t rows, int32_t width, wgs_dtype dtype,
+                                                 cudaStream_t stream) {
+    const wgs_status st = bias_gelu_bwd_args(grad_y, x, bias, grad_x, grad_bias, rows, width, dtype);
+    if (st != WGS_OK || width == 0) return st;
+    if (bwd_workspace_bytes(rows > 0 ? rows : 1, width) > kNoAllocScratchFloats * sizeof(float))
+        return WGS_ERR_TOO_LARGE;
+    DeviceInfo dev;
+    const wgs_status ds = current_device(&dev);
+    if (ds != WGS_OK) return ds;
+    float *scratch = nullptr;
+    const wgs_status ss = scratch_for(dev.device, &scratch);
+    if (ss != WGS_OK) return ss;
+    // Pass 1 writes every partial sum that pass 2 reads, in stream order, so
+    // nothing in the array needs clearing between calls.
+    return bias_gelu_bwd_checked(grad_y, x, bias, grad_x, grad_bias, scratch, rows, width, dtype,
+                                 stream);
 }

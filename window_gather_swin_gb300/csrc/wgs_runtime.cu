@@ -48,6 +48,7 @@ extern "C" const char *wgs_status_string(wgs_status s) {
         case WGS_ERR_INDEX: return "a gather index was outside [-1, n_src)";
         case WGS_ERR_ALIAS: return "buffers overlap in a way the operation does not allow";
         case WGS_ERR_CUDA: return "a CUDA runtime call failed";
+        case WGS_ERR_TOO_LARGE: return "problem larger than the library's fixed scratch array";
     }
     return "unknown status";
 }
