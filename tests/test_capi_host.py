@@ -225,7 +225,7 @@ def test_block_boundary_argument_errors(lib):
 def test_gelu_backward_argument_errors(lib):
     f = lib.bias_gelu_tanh_bwd
     need = lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 768)
-    assert need == 16 * 768 * 4                      # 1000 rows -> 16 slabs of >= 64 rows
+    assert need == 8 * 768 * 4                       # 1000 rows -> 8 slabs of >= 128 rows
     assert lib.wgs_bias_gelu_bwd_workspace_bytes(131040, 768) == 512 * 768 * 4
     assert lib.wgs_bias_gelu_bwd_workspace_bytes(0, 768) == 0
     W = 0x50000000

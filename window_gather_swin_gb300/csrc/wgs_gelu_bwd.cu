@@ -17,7 +17,8 @@
 //      of its slab, stores grad_x and accumulates the rounded gradients in
 //      FP32 registers; the G row groups of the CTA then combine in shared
 //      memory in a fixed order into partial[slab][column];
-//   2. one thread per column sums partial[0..slabs) in order.
+//   2. per column, 16 lanes sum interleaved slabs in order and then combine
+//      in lane order (gelu_bwd_bias).
 // The slab count depends only on the row count, so results do not depend
 // on the device.  Both passes stream: grad_y and x are read once and grad_x
 // is written once; the partials are a few MB at most.
@@ -26,6 +27,16 @@
 #include <type_traits>
 
 #include "wgs_common.cuh"
+
+#ifndef WGS_BWD_ROWS
+#define WGS_BWD_ROWS 4  // rows in flight per thread per iteration
+#endif
+#ifndef WGS_BWD_GROUPS
+#define WGS_BWD_GROUPS 1  // most row groups per CTA
+#endif
+#ifndef WGS_BWD_MIN_SLAB_ROWS
+#define WGS_BWD_MIN_SLAB_ROWS 128  // rows per slab at least (slab count = min(512, rows / this))
+#endif
 
 namespace wgs {
 
@@ -36,7 +47,7 @@ struct F32 {};
 constexpr double kSqrt2OverPi = 0.7978845608028654;
 constexpr double kLog2e = 1.4426950408889634;
 constexpr float kFarLeft = -4.0f;
-constexpr int64_t kMinRowsPerSlab = 64;
+constexpr int64_t kMinRowsPerSlab = WGS_BWD_MIN_SLAB_ROWS;
 constexpr int64_t kMaxSlabs = 512;
 constexpr int kMaxChunksPerBlock = 256;  // column chunks per CTA
 constexpr int kMaxThreads = 512;
@@ -63,34 +74,76 @@ __device__ __noinline__ float gelu_grad_far_left(float t) {
     return static_cast<float>(s + td * s * one_minus_s * (2.0 * k) * (1.0 + 3.0 * 0.044715 * td * td));
 }
 
-__device__ __forceinline__ float gelu_grad(float t) {
+// Valid for t >= kFarLeft (and +inf / NaN, which give NaN like the FP64 form).
+__device__ __forceinline__ float gelu_grad_fast(float t) {
     constexpr float c1 = static_cast<float>(-2.0 * kSqrt2OverPi * kLog2e);
     constexpr float c3 = static_cast<float>(-2.0 * kSqrt2OverPi * 0.044715 * kLog2e);
     constexpr float k1 = static_cast<float>(2.0 * kSqrt2OverPi);
     constexpr float k3 = static_cast<float>(6.0 * kSqrt2OverPi * 0.044715);
-    if (t < kFarLeft) return gelu_grad_far_left(t);
     const float t2 = t * t;
     const float e = ex2_approx(t * fmaf(c3, t2, c1));
     const float s = rcp_approx(1.0f + e);
     return fmaf(t * s * (e * s), fmaf(k3, t2, k1), s);
 }
 
-// Gradient of the two 16-bit elements of one word: returns the rounded
-// grad_x word and adds the rounded values to acc[0..1].
-template <typename E>
-__device__ __forceinline__ uint32_t grad_word16(uint32_t gy, uint32_t x, uint32_t b, float *acc) {
-    const float2 t = E::to_f2(E::add2(x, b));
-    const float2 g = E::to_f2(gy);
-    const uint32_t r = E::from_f2(g.x * gelu_grad(t.x), g.y * gelu_grad(t.y));
-    const float2 rv = E::to_f2(r);
-    acc[0] += rv.x;
-    acc[1] += rv.y;
-    return r;
+__device__ __forceinline__ float gelu_grad(float t) {
+    return t < kFarLeft ? gelu_grad_far_left(t) : gelu_grad_fast(t);
+}
+
+// One 16-byte chunk: grad_x = round(gy * gelu'(round(x + b))) for its 4 or
+// 8 elements, and the rounded values added to acc.  The fast form runs on
+// every element; the rare far-left elements are redone behind one branch.
+template <typename E, bool k16>
+__device__ __forceinline__ uint4 grad_chunk(const uint4 &gyv, const uint4 &xv, const uint4 &bv,
+                                            float *acc) {
+    constexpr int kN = k16 ? 8 : 4;
+    float t[kN], g[kN], d[kN];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        if constexpr (k16) {
+            const float2 tf = E::to_f2(E::add2(word(xv, w), word(bv, w)));
+            const float2 gf = E::to_f2(word(gyv, w));
+            t[2 * w] = tf.x;
+            t[2 * w + 1] = tf.y;
+            g[2 * w] = gf.x;
+            g[2 * w + 1] = gf.y;
+        } else {
+            t[w] = __uint_as_float(word(xv, w)) + __uint_as_float(word(bv, w));
+            g[w] = __uint_as_float(word(gyv, w));
+        }
+    }
+    float lowest = t[0];
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+        d[e] = gelu_grad_fast(t[e]);
+        lowest = fminf(lowest, t[e]);
+    }
+    if (lowest < kFarLeft) {
+#pragma unroll
+        for (int e = 0; e < kN; ++e)
+            if (t[e] < kFarLeft) d[e] = gelu_grad_far_left(t[e]);
+    }
+    uint4 out;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        if constexpr (k16) {
+            const uint32_t r = E::from_f2(g[2 * w] * d[2 * w], g[2 * w + 1] * d[2 * w + 1]);
+            const float2 rv = E::to_f2(r);
+            acc[2 * w] += rv.x;
+            acc[2 * w + 1] += rv.y;
+            set_word(out, w, r);
+        } else {
+            const float v = g[w] * d[w];
+            acc[w] += v;
+            set_word(out, w, __float_as_uint(v));
+        }
+    }
+    return out;
 }
 
 // Pass 1, 16-byte chunks.  Block = CVB * G threads: thread (g, j) owns
 // column chunk blockIdx.y * CVB + j and walks every G-th row of the slab.
-template <typename E>
+template <typename E, int R>
 __global__ void __launch_bounds__(kMaxThreads)
 gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
                 int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
@@ -108,54 +161,23 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     for (int e = 0; e < kN; ++e) acc[e] = 0.f;
     if (active) {
         const uint4 bv = __ldg(bias + cv);
-        int64_t r = r0 + g;
-        // two rows in flight per iteration
-        for (; r + groups < r1; r += 2 * groups) {
-            const int64_t i0 = r * row_chunks + cv, i1 = (r + groups) * row_chunks + cv;
-            const uint4 gy0 = ld_stream(gy + i0), x0 = ld_stream(x + i0);
-            const uint4 gy1 = ld_stream(gy + i1), x1 = ld_stream(x + i1);
-            uint4 o0, o1;
+        // R rows in flight per iteration; accumulation order is by row
+        for (int64_t r = r0 + g; r < r1; r += static_cast<int64_t>(R) * groups) {
+            uint4 gyv[R], xv[R];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                if constexpr (k16) {
-                    set_word(o0, w, grad_word16<E>(word(gy0, w), word(x0, w), word(bv, w), acc + 2 * w));
-                } else {
-                    const float t = __uint_as_float(word(x0, w)) + __uint_as_float(word(bv, w));
-                    const float v = __uint_as_float(word(gy0, w)) * gelu_grad(t);
-                    acc[w] += v;
-                    set_word(o0, w, __float_as_uint(v));
+            for (int q = 0; q < R; ++q) {
+                const int64_t rr = r + static_cast<int64_t>(q) * groups;
+                if (rr < r1) {
+                    gyv[q] = ld_stream(gy + rr * row_chunks + cv);
+                    xv[q] = ld_stream(x + rr * row_chunks + cv);
                 }
             }
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                if constexpr (k16) {
-                    set_word(o1, w, grad_word16<E>(word(gy1, w), word(x1, w), word(bv, w), acc + 2 * w));
-                } else {
-                    const float t = __uint_as_float(word(x1, w)) + __uint_as_float(word(bv, w));
-                    const float v = __uint_as_float(word(gy1, w)) * gelu_grad(t);
-                    acc[w] += v;
-                    set_word(o1, w, __float_as_uint(v));
-                }
+            for (int q = 0; q < R; ++q) {
+                const int64_t rr = r + static_cast<int64_t>(q) * groups;
+                if (rr < r1)
+                    st_stream(gx + rr * row_chunks + cv, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
             }
-            st_stream(gx + i0, o0);
-            st_stream(gx + i1, o1);
-        }
-        if (r < r1) {
-            const int64_t i0 = r * row_chunks + cv;
-            const uint4 gy0 = ld_stream(gy + i0), x0 = ld_stream(x + i0);
-            uint4 o0;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                if constexpr (k16) {
-                    set_word(o0, w, grad_word16<E>(word(gy0, w), word(x0, w), word(bv, w), acc + 2 * w));
-                } else {
-                    const float t = __uint_as_float(word(x0, w)) + __uint_as_float(word(bv, w));
-                    const float v = __uint_as_float(word(gy0, w)) * gelu_grad(t);
-                    acc[w] += v;
-                    set_word(o0, w, __float_as_uint(v));
-                }
-            }
-            st_stream(gx + i0, o0);
         }
     }
     // combine the row groups in a fixed order
@@ -216,19 +238,43 @@ gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, floa
     }
 }
 
-// Pass 2: grad_bias[c] = round(sum over slabs of partial[slab][c]), in slab order.
+// Pass 2: grad_bias[c] = round(sum over slabs of partial[slab][c]).  A CTA
+// takes 32 columns; its 16 slab lanes each sum slabs k, k + 16, ... in order
+// (8 loads in flight, each warp reading 32 consecutive columns of a slab),
+// then lane sums combine in lane order.  The order is fixed, so the result
+// is deterministic.
+constexpr int kBiasCols = 32, kBiasLanes = 16;
+
 template <typename E>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kBiasCols * kBiasLanes)
 gelu_bwd_bias(const float *partial, void *grad_bias, int32_t width, int32_t slabs) {
     pdl_prologue();
-    const int32_t c = static_cast<int32_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= width) return;
+    __shared__ float red[kBiasLanes][kBiasCols];
+    const int col = threadIdx.x % kBiasCols, lane = threadIdx.x / kBiasCols;
+    const int32_t c = static_cast<int32_t>(blockIdx.x) * kBiasCols + col;
     float s = 0.f;
-    for (int32_t q = 0; q < slabs; ++q) s += partial[static_cast<int64_t>(q) * width + c];
-    if constexpr (std::is_same<E, F32>::value)
-        static_cast<float *>(grad_bias)[c] = s;
-    else
-        static_cast<uint16_t *>(grad_bias)[c] = static_cast<uint16_t>(E::from_f2(s, 0.f));
+    if (c < width) {
+        int32_t q = lane;
+        for (; q + 7 * kBiasLanes < slabs; q += 8 * kBiasLanes) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = __ldcg(partial + static_cast<int64_t>(q + u * kBiasLanes) * width + c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        for (; q < slabs; q += kBiasLanes) s += __ldcg(partial + static_cast<int64_t>(q) * width + c);
+    }
+    red[lane][col] = s;
+    __syncthreads();
+    if (lane == 0 && c < width) {
+        float t = red[0][col];
+        for (int k = 1; k < kBiasLanes; ++k) t += red[k][col];
+        if constexpr (std::is_same<E, F32>::value)
+            static_cast<float *>(grad_bias)[c] = t;
+        else
+            static_cast<uint16_t *>(grad_bias)[c] = static_cast<uint16_t>(E::from_f2(t, 0.f));
+    }
 }
 
 int64_t slabs_for(int64_t rows) {
@@ -247,14 +293,14 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
     const int32_t units = chunks ? width / kVec : width;        // column units per row
     const int32_t cvb = units < kMaxChunksPerBlock ? units : kMaxChunksPerBlock;
     int32_t groups = kMaxThreads / cvb;
-    if (groups > 8) groups = 8;
+    if (groups > WGS_BWD_GROUPS) groups = WGS_BWD_GROUPS;
     if (groups < 1) groups = 1;
     const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ceil_div(units, cvb)));
     const dim3 block(static_cast<unsigned>(cvb * groups));
     wgs_status st;
     if (chunks) {
         const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
-        st = launch(gelu_bwd_chunks<E>, grid, block, smem, stream, static_cast<const uint4 *>(gy),
+        st = launch(gelu_bwd_chunks<E, WGS_BWD_ROWS>, grid, block, smem, stream, static_cast<const uint4 *>(gy),
                     static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
                     static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups, slabs);
     } else {
@@ -263,8 +309,9 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
                     width, cvb, groups, slabs);
     }
     if (st != WGS_OK) return st;
-    return launch(gelu_bwd_bias<E>, dim3(static_cast<unsigned>(ceil_div(width, 256))), dim3(256), 0,
-                  stream, static_cast<const float *>(partial), gb, width, slabs);
+    return launch(gelu_bwd_bias<E>, dim3(static_cast<unsigned>(ceil_div(width, kBiasCols))),
+                  dim3(kBiasCols * kBiasLanes), 0, stream, static_cast<const float *>(partial), gb,
+                  width, slabs);
 }
 
 }  // namespace
