@@ -235,8 +235,9 @@ wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows
  *     grad_x    = round(grad_y * gelu'(t))   (gelu' evaluated in FP32)
  *     grad_bias = round(sum over rows of grad_x[., c])       (FP32 sum)
  * The column sum is deterministic: per-slab FP32 partial sums go to
- * `workspace`, then one pass adds them in a fixed order; the slab count
- * depends only on `rows`, so results do not depend on the device.
+ * `workspace`, then one pass adds them in a fixed order; the summation
+ * order depends only on rows, width and dtype, so results do not depend on
+ * the device.
  *   grad_y, x, grad_x  [rows, width] of `dtype`; grad_x may equal grad_y,
  *          other overlaps return WGS_ERR_ALIAS.
  *   bias, grad_bias    [width] of `dtype`, disjoint from everything else.

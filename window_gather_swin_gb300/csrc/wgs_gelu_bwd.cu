@@ -11,17 +11,24 @@
 //     gelu'(t) = s + t s (1 - s) (2k + 6k a t^2),   k = sqrt(2/pi), a = 0.044715.
 // Below t = -4 the FP64 form runs, as in the forward.
 //
+// The FP32 arithmetic of gelu' runs two elements per instruction on the
+// packed FP32 pipe (__fmul2_rn and friends: each lane is the correctly
+// rounded scalar operation), which roughly halves the instructions per
+// element; the kernel must stay HBM-bound with eight fp16 elements per
+// 16-byte load.
+//
 // The column sum is deterministic and runs in two passes:
 //   1. grid (slab, column block): every thread owns one 16-byte column chunk
 //      (or one column on the scalar path), walks rows r0 + g, r0 + g + G, ...
 //      of its slab, stores grad_x and accumulates the rounded gradients in
 //      FP32 registers; the G row groups of the CTA then combine in shared
 //      memory in a fixed order into partial[slab][column];
-//   2. per column, 16 lanes sum interleaved slabs in order and then combine
+//   2. per column, 32 lanes sum interleaved slabs in order and then combine
 //      in lane order (gelu_bwd_bias).
-// The slab count depends only on the row count, so results do not depend
-// on the device.  Both passes stream: grad_y and x are read once and grad_x
-// is written once; the partials are a few MB at most.
+// The slab count depends only on the row count and G only on the shape and
+// format, so results do not depend on the device.  Both passes stream:
+// grad_y and x are read once and grad_x is written once; the partials are a
+// few MB at most.
 #include <atomic>
 #include <mutex>
 #include <type_traits>
@@ -29,10 +36,19 @@
 #include "wgs_common.cuh"
 
 #ifndef WGS_BWD_ROWS
-#define WGS_BWD_ROWS 4  // rows in flight per thread per iteration
+#define WGS_BWD_ROWS 4  // rows in flight per thread, fp32
+#endif
+#ifndef WGS_BWD_ROWS16
+#define WGS_BWD_ROWS16 3  // rows in flight per thread, 16-bit formats
 #endif
 #ifndef WGS_BWD_GROUPS
-#define WGS_BWD_GROUPS 1  // most row groups per CTA
+#define WGS_BWD_GROUPS 4  // most row groups per CTA
+#endif
+#ifndef WGS_BWD_TARGET_THREADS
+#define WGS_BWD_TARGET_THREADS 98304  // pass-1 threads to aim for when choosing row groups
+#endif
+#ifndef WGS_BWD_MIN_BLOCKS
+#define WGS_BWD_MIN_BLOCKS 2  // pass-1 CTAs of the largest size kept resident per SM
 #endif
 #ifndef WGS_BWD_MIN_SLAB_ROWS
 #define WGS_BWD_MIN_SLAB_ROWS 128  // rows per slab at least (slab count = min(512, rows / this))
@@ -50,7 +66,11 @@ constexpr float kFarLeft = -4.0f;
 constexpr int64_t kMinRowsPerSlab = WGS_BWD_MIN_SLAB_ROWS;
 constexpr int64_t kMaxSlabs = 512;
 constexpr int kMaxChunksPerBlock = 256;  // column chunks per CTA
-constexpr int kMaxThreads = 512;
+// Pass 1 runs at most 384 threads per CTA and keeps two such CTAs per SM
+// resident (at most 85 registers a thread), so the usual grids fit in one
+// wave.
+constexpr int kMaxThreads = 384;
+constexpr int kMinBlocks = WGS_BWD_MIN_BLOCKS;
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float r;
@@ -86,65 +106,100 @@ __device__ __forceinline__ float gelu_grad_fast(float t) {
     return fmaf(t * s * (e * s), fmaf(k3, t2, k1), s);
 }
 
+// gelu_grad_fast of two elements, on the packed FP32 pipe (each lane is the
+// correctly rounded scalar operation, in the same order).
+__device__ __forceinline__ float2 gelu_grad_fast2(float2 t) {
+    constexpr float c1 = static_cast<float>(-2.0 * kSqrt2OverPi * kLog2e);
+    constexpr float c3 = static_cast<float>(-2.0 * kSqrt2OverPi * 0.044715 * kLog2e);
+    constexpr float k1 = static_cast<float>(2.0 * kSqrt2OverPi);
+    constexpr float k3 = static_cast<float>(6.0 * kSqrt2OverPi * 0.044715);
+    const float2 t2 = __fmul2_rn(t, t);
+    const float2 w = __fmul2_rn(t, __ffma2_rn(make_float2(c3, c3), t2, make_float2(c1, c1)));
+    const float2 e = make_float2(ex2_approx(w.x), ex2_approx(w.y));
+    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), e);
+    const float2 s = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    const float2 ts_es = __fmul2_rn(__fmul2_rn(t, s), __fmul2_rn(e, s));
+    return __ffma2_rn(ts_es, __ffma2_rn(make_float2(k3, k3), t2, make_float2(k1, k1)), s);
+}
+
 __device__ __forceinline__ float gelu_grad(float t) {
     return t < kFarLeft ? gelu_grad_far_left(t) : gelu_grad_fast(t);
 }
 
+// Element pair w of a chunk as FP32: t = round(x + b) and g = grad_y, for
+// 16-bit words (one pair per word) or fp32 words (pair = words 2w, 2w + 1).
+template <typename E, bool k16>
+__device__ __forceinline__ void chunk_pair(const uint4 &gyv, const uint4 &xv, const uint4 &bv,
+                                           int w, float2 &t, float2 &g) {
+    if constexpr (k16) {
+        t = E::to_f2(E::add2(word(xv, w), word(bv, w)));
+        g = E::to_f2(word(gyv, w));
+    } else {
+        t = make_float2(__uint_as_float(word(xv, 2 * w)) + __uint_as_float(word(bv, 2 * w)),
+                        __uint_as_float(word(xv, 2 * w + 1)) + __uint_as_float(word(bv, 2 * w + 1)));
+        g = make_float2(__uint_as_float(word(gyv, 2 * w)), __uint_as_float(word(gyv, 2 * w + 1)));
+    }
+}
+
+// Store the pair v = grad_x of pair w into out (rounded for 16-bit words).
+template <typename E, bool k16>
+__device__ __forceinline__ void put_pair(uint4 &out, int w, float2 v) {
+    if constexpr (k16) {
+        set_word(out, w, E::from_f2(v.x, v.y));
+    } else {
+        set_word(out, 2 * w, __float_as_uint(v.x));
+        set_word(out, 2 * w + 1, __float_as_uint(v.y));
+    }
+}
+
+// The chunk with gelu_grad chosen per element (far-left elements in FP64);
+// only chunks holding some t < -4 come here.
+template <typename E, bool k16>
+__device__ __forceinline__ uint4 grad_chunk_exact(uint4 gyv, uint4 xv, uint4 bv) {
+    uint4 out;
+    for (int w = 0; w < (k16 ? 4 : 2); ++w) {
+        float2 t, g;
+        chunk_pair<E, k16>(gyv, xv, bv, w, t, g);
+        put_pair<E, k16>(out, w, make_float2(g.x * gelu_grad(t.x), g.y * gelu_grad(t.y)));
+    }
+    return out;
+}
+
 // One 16-byte chunk: grad_x = round(gy * gelu'(round(x + b))) for its 4 or
-// 8 elements, and the rounded values added to acc.  The fast form runs on
-// every element; the rare far-left elements are redone behind one branch.
+// 8 elements, and the rounded values added to acc.  The packed fast form
+// runs on every pair; a chunk with a far-left element is redone by
+// grad_chunk_exact, which gives the same bits everywhere else.
 template <typename E, bool k16>
 __device__ __forceinline__ uint4 grad_chunk(const uint4 &gyv, const uint4 &xv, const uint4 &bv,
-                                            float *acc) {
-    constexpr int kN = k16 ? 8 : 4;
-    float t[kN], g[kN], d[kN];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        if constexpr (k16) {
-            const float2 tf = E::to_f2(E::add2(word(xv, w), word(bv, w)));
-            const float2 gf = E::to_f2(word(gyv, w));
-            t[2 * w] = tf.x;
-            t[2 * w + 1] = tf.y;
-            g[2 * w] = gf.x;
-            g[2 * w + 1] = gf.y;
-        } else {
-            t[w] = __uint_as_float(word(xv, w)) + __uint_as_float(word(bv, w));
-            g[w] = __uint_as_float(word(gyv, w));
-        }
-    }
-    float lowest = t[0];
-#pragma unroll
-    for (int e = 0; e < kN; ++e) {
-        d[e] = gelu_grad_fast(t[e]);
-        lowest = fminf(lowest, t[e]);
-    }
-    if (lowest < kFarLeft) {
-#pragma unroll
-        for (int e = 0; e < kN; ++e)
-            if (t[e] < kFarLeft) d[e] = gelu_grad_far_left(t[e]);
-    }
+                                            float2 *acc) {
+    constexpr int kPairs = k16 ? 4 : 2;
     uint4 out;
+    float lowest = INFINITY;  // NaN needs no redo: the fast form gives NaN too
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        if constexpr (k16) {
-            const uint32_t r = E::from_f2(g[2 * w] * d[2 * w], g[2 * w + 1] * d[2 * w + 1]);
-            const float2 rv = E::to_f2(r);
-            acc[2 * w] += rv.x;
-            acc[2 * w + 1] += rv.y;
-            set_word(out, w, r);
-        } else {
-            const float v = g[w] * d[w];
-            acc[w] += v;
-            set_word(out, w, __float_as_uint(v));
-        }
+    for (int w = 0; w < kPairs; ++w) {
+        float2 t, g;
+        chunk_pair<E, k16>(gyv, xv, bv, w, t, g);
+        put_pair<E, k16>(out, w, __fmul2_rn(g, gelu_grad_fast2(t)));
+        lowest = fminf(lowest, fminf(t.x, t.y));
+    }
+    if (lowest < kFarLeft) out = grad_chunk_exact<E, k16>(gyv, xv, bv);
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) {
+        if constexpr (k16)
+            acc[w] = __fadd2_rn(acc[w], E::to_f2(word(out, w)));
+        else
+            acc[w] = __fadd2_rn(acc[w], make_float2(__uint_as_float(word(out, 2 * w)),
+                                                    __uint_as_float(word(out, 2 * w + 1))));
     }
     return out;
 }
 
 // Pass 1, 16-byte chunks.  Block = CVB * G threads: thread (g, j) owns
-// column chunk blockIdx.y * CVB + j and walks every G-th row of the slab.
+// column chunk blockIdx.y * CVB + j and walks rows r0 + g, r0 + g + G, ...
+// of its slab, R rows in flight at a time, accumulating them in
+// increasing row order.
 template <typename E, int R>
-__global__ void __launch_bounds__(kMaxThreads)
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
                 int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
                 int32_t slabs) {
@@ -156,17 +211,17 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     const int32_t cv = static_cast<int32_t>(blockIdx.y) * cvb + j;
     const bool active = g < groups && cv < row_chunks;
     const int64_t r0 = rows * blockIdx.x / slabs, r1 = rows * (blockIdx.x + 1) / slabs;
-    float acc[kN];
+    float2 acc[kN / 2];
 #pragma unroll
-    for (int e = 0; e < kN; ++e) acc[e] = 0.f;
+    for (int e = 0; e < kN / 2; ++e) acc[e] = make_float2(0.f, 0.f);
     if (active) {
         const uint4 bv = __ldg(bias + cv);
-        // R rows in flight per iteration; accumulation order is by row
-        for (int64_t r = r0 + g; r < r1; r += static_cast<int64_t>(R) * groups) {
+        const int64_t G = groups;
+        for (int64_t r = r0 + g; r < r1; r += R * G) {
             uint4 gyv[R], xv[R];
 #pragma unroll
             for (int q = 0; q < R; ++q) {
-                const int64_t rr = r + static_cast<int64_t>(q) * groups;
+                const int64_t rr = r + q * G;
                 if (rr < r1) {
                     gyv[q] = ld_stream(gy + rr * row_chunks + cv);
                     xv[q] = ld_stream(x + rr * row_chunks + cv);
@@ -174,7 +229,7 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
             }
 #pragma unroll
             for (int q = 0; q < R; ++q) {
-                const int64_t rr = r + static_cast<int64_t>(q) * groups;
+                const int64_t rr = r + q * G;
                 if (rr < r1)
                     st_stream(gx + rr * row_chunks + cv, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
             }
@@ -183,7 +238,7 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     // combine the row groups in a fixed order
     if (g < groups)
 #pragma unroll
-        for (int e = 0; e < kN; ++e) red[(g * cvb + j) * kN + e] = acc[e];
+        for (int e = 0; e < kN; ++e) red[(g * cvb + j) * kN + e] = e & 1 ? acc[e / 2].y : acc[e / 2].x;
     __syncthreads();
     if (g == 0 && cv < row_chunks) {
 #pragma unroll
@@ -197,7 +252,7 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
 
 // Pass 1, any width / alignment: thread (g, j) owns column blockIdx.y*CVB + j.
 template <typename E>
-__global__ void __launch_bounds__(kMaxThreads)
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, float *partial,
                 int64_t rows, int32_t width, int32_t cvb, int32_t groups, int32_t slabs) {
     pdl_prologue();
@@ -239,11 +294,11 @@ gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, floa
 }
 
 // Pass 2: grad_bias[c] = round(sum over slabs of partial[slab][c]).  A CTA
-// takes 32 columns; its 16 slab lanes each sum slabs k, k + 16, ... in order
-// (8 loads in flight, each warp reading 32 consecutive columns of a slab),
-// then lane sums combine in lane order.  The order is fixed, so the result
-// is deterministic.
-constexpr int kBiasCols = 32, kBiasLanes = 16;
+// takes 32 columns; its 32 slab lanes (one warp each, reading 32
+// consecutive columns of a slab) each sum slabs k, k + 32, ... in order,
+// 16 loads in flight, then the lane sums combine in lane order.  The order
+// is fixed, so the result is deterministic.
+constexpr int kBiasCols = 32, kBiasLanes = 32, kBiasUnroll = 16;
 
 template <typename E>
 __global__ void __launch_bounds__(kBiasCols * kBiasLanes)
@@ -255,13 +310,13 @@ gelu_bwd_bias(const float *partial, void *grad_bias, int32_t width, int32_t slab
     float s = 0.f;
     if (c < width) {
         int32_t q = lane;
-        for (; q + 7 * kBiasLanes < slabs; q += 8 * kBiasLanes) {
-            float v[8];
+        for (; q + (kBiasUnroll - 1) * kBiasLanes < slabs; q += kBiasUnroll * kBiasLanes) {
+            float v[kBiasUnroll];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < kBiasUnroll; ++u)
                 v[u] = __ldcg(partial + static_cast<int64_t>(q + u * kBiasLanes) * width + c);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) s += v[u];
+            for (int u = 0; u < kBiasUnroll; ++u) s += v[u];
         }
         for (; q < slabs; q += kBiasLanes) s += __ldcg(partial + static_cast<int64_t>(q) * width + c);
     }
@@ -292,17 +347,22 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
                         aligned16(gx);
     const int32_t units = chunks ? width / kVec : width;        // column units per row
     const int32_t cvb = units < kMaxChunksPerBlock ? units : kMaxChunksPerBlock;
-    int32_t groups = kMaxThreads / cvb;
-    if (groups > WGS_BWD_GROUPS) groups = WGS_BWD_GROUPS;
-    if (groups < 1) groups = 1;
-    const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ceil_div(units, cvb)));
+    const int64_t col_blocks = ceil_div(units, cvb);
+    // Row groups: enough threads to cover the GPU's memory latency, chosen
+    // from the shape alone (the summation order depends on it).
+    int64_t groups64 = WGS_BWD_TARGET_THREADS / (static_cast<int64_t>(slabs) * col_blocks * cvb);
+    if (groups64 > WGS_BWD_GROUPS) groups64 = WGS_BWD_GROUPS;
+    if (groups64 > kMaxThreads / cvb) groups64 = kMaxThreads / cvb;
+    const int32_t groups = groups64 < 1 ? 1 : static_cast<int32_t>(groups64);
+    const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(col_blocks));
     const dim3 block(static_cast<unsigned>(cvb * groups));
     wgs_status st;
     if (chunks) {
         const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
-        st = launch(gelu_bwd_chunks<E, WGS_BWD_ROWS>, grid, block, smem, stream, static_cast<const uint4 *>(gy),
-                    static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
-                    static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups, slabs);
+        st = launch(gelu_bwd_chunks<E, k16 ? WGS_BWD_ROWS16 : WGS_BWD_ROWS>, grid, block, smem, stream,
+                    static_cast<const uint4 *>(gy), static_cast<const uint4 *>(x),
+                    static_cast<const uint4 *>(bias), static_cast<uint4 *>(gx), partial, rows,
+                    units, width, cvb, groups, slabs);
     } else {
         const size_t smem = static_cast<size_t>(groups) * cvb * sizeof(float);
         st = launch(gelu_bwd_scalar<E>, grid, block, smem, stream, gy, x, bias, gx, partial, rows,
