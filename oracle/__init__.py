@@ -1,5 +1,6 @@
 """CPU oracle for the block-glue path (LN, residual add + LN, window index
-map, window gather, norm-gather, bias + tanh-GELU).
+map, window gather, norm-gather, bias + tanh-GELU and its backward, the
+shifted-window attention bias-mask add).
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 benchmark's CPU-baseline leg import this package; the library in
@@ -57,6 +58,9 @@ def _load():
             "orc_bias_gelu_f32": (None, [P, P, P, P, i64, i32]),
             "orc_bias_gelu_bwd": (None, [P, P, P, P, P, P, P, i64, i32, ctypes.c_int]),
             "orc_bias_gelu_f16": (None, [P, P, P, P, i64, i32]),
+            "orc_build_shift_regions": (ctypes.c_int, [P, P, P, P, i32, i32, P]),
+            "orc_window_bias_mask_add_fmt": (None, [P, P, P, P, P, i64, i32, i32, ctypes.c_double,
+                                                    ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -294,3 +298,38 @@ def bias_gelu_tanh_bwd(grad_y, x, bias, fmt: str = None):
     _load().orc_bias_gelu_bwd(_ptr(gy), _ptr(xs), _ptr(bs), _ptr(gx), _ptr(gb), _ptr(gx64),
                               _ptr(gb64), rows, width, code)
     return gx, gb, gx64, gb64
+
+
+# ------------------------------------------------------------ bias-mask ----
+
+def build_shift_regions(grid, win, shift, padded=None, flags: int = 0, axes_mask: int = 7):
+    """INT32 region label of every windowed row (window-major order): bit k
+    set when the row's cell lies past the roll's seam along masked axis k."""
+    n = window_index_count(grid, win, padded)
+    out = np.empty(n, dtype=np.int32)
+    rc = _load().orc_build_shift_regions(_ptr(_i3(grid)), _ptr(_i3(win)), _ptr(_i3(shift)),
+                                         _ptr(_i3(padded)), flags, axes_mask, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_build_shift_regions failed ({rc})")
+    return out
+
+
+def window_bias_mask_add(scores, bias, win_type=None, region=None, mask_value: float = -100.0,
+                         fmt: str = "f16"):
+    """out = round(round(scores + bias[type]) + m), m = 0 / mask_value by
+    region labels (no mask add without labels).  scores [n_win, heads, n, n],
+    bias [n_types, heads, n, n]; float16 arrays, or uint16 bits with
+    fmt="bf16"."""
+    code, dt = _fmt(fmt)
+    s = _c(scores, dt)
+    b = _c(bias, dt)
+    n_win, heads, n, n2 = s.shape
+    assert n == n2 and b.ndim == 4 and b.shape[1:] == (heads, n, n)
+    t = None if win_type is None else _c(win_type, np.int32).ravel()
+    r = None if region is None else _c(region, np.int32).ravel()
+    assert t is None or (t.size == n_win and ((t >= 0) & (t < b.shape[0])).all())
+    assert r is None or r.size == n_win * n
+    out = np.empty_like(s)
+    _load().orc_window_bias_mask_add_fmt(_ptr(s), _ptr(b), _ptr(t), _ptr(r), _ptr(out), n_win,
+                                         heads, n, float(mask_value), code)
+    return out

@@ -585,3 +585,102 @@ void orc_bias_gelu_bwd(const void *grad_y, const void *x, const void *bias, void
     }
     free(sum);
 }
+
+/* ------------------------------------------------------------------ */
+/* Shifted-window attention bias and mask ("bias-mask")  [P1 s7]       */
+/* ------------------------------------------------------------------ */
+/* [P1 s7] names a "bias-mask" op among the kernels kept in the final
+ * combination and s6 rejects fusing it with softmax; neither gives its
+ * arithmetic.  The reading here is the shifted-window transformer's
+ * general one (Swin): before softmax the attention logits of every window
+ * and head get a position bias and, for shifted blocks, a mask that keeps
+ * tokens from attending across a seam that the cyclic roll created.
+ *
+ * Region labels.  Along axis k a windowed row's cell c (its coordinate in
+ * the rolled, padded grid) holds the token rolled in from coordinate
+ * c + s_k of the period (the grid, or the padded grid for pad-then-shift);
+ * when the roll moves that axis (s_k mod period_k != 0) the cell lies past
+ * the seam if c + s_k >= period_k.  The label of a
+ * row is the sum over the masked axes (bit k of axes_mask) of
+ * 2^k * [past the seam along k].  Pad cells are labelled by the same rule.
+ * Labels come out in the window-major destination order of
+ * orc_build_window_index; like that builder this one scatters from every
+ * padded cell to its destination row. */
+int orc_build_shift_regions(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                            const int32_t *padded, int32_t flags, int32_t axes_mask,
+                            int32_t *out)
+{
+    int64_t P[3];
+    if (resolve_padded(grid, win, padded, P) != 0) return -1;
+    if (flags != 0 && flags != 1) return -1;
+    int64_t period[3], s[3], nwin[3];
+    for (int k = 0; k < 3; ++k) {
+        period[k] = flags == 1 ? P[k] : (int64_t)grid[k];
+        s[k] = pos_mod(shift[k], period[k]);
+        nwin[k] = ceil_div64(P[k], win[k]);
+    }
+    /* rows before each window: the same window-major order as the index map */
+    int64_t n_windows = nwin[0] * nwin[1] * nwin[2];
+    int64_t *start = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_windows + 1));
+    if (!start) return -2;
+    start[0] = 0;
+    for (int64_t w_id = 0; w_id < n_windows; ++w_id) {
+        int64_t bz = w_id / (nwin[1] * nwin[2]), bh = (w_id / nwin[2]) % nwin[1], bw = w_id % nwin[2];
+        int64_t e[3] = {P[0] - bz * win[0], P[1] - bh * win[1], P[2] - bw * win[2]};
+        for (int k = 0; k < 3; ++k) if (e[k] > win[k]) e[k] = win[k];
+        start[w_id + 1] = start[w_id] + e[0] * e[1] * e[2];
+    }
+    for (int64_t z = 0; z < P[0]; ++z)
+        for (int64_t h = 0; h < P[1]; ++h)
+            for (int64_t w = 0; w < P[2]; ++w) {
+                const int64_t c[3] = {z, h, w};
+                int64_t b[3], e[3], i[3];
+                for (int k = 0; k < 3; ++k) {
+                    b[k] = c[k] / win[k];
+                    i[k] = c[k] % win[k];
+                    e[k] = P[k] - b[k] * win[k];
+                    if (e[k] > win[k]) e[k] = win[k];
+                }
+                int64_t w_id = (b[0] * nwin[1] + b[1]) * nwin[2] + b[2];
+                int64_t dst = start[w_id] + (i[0] * e[1] + i[1]) * e[2] + i[2];
+                int32_t label = 0;
+                for (int k = 0; k < 3; ++k)
+                    if (((axes_mask >> k) & 1) && s[k] != 0)
+                        label += (c[k] + s[k] >= period[k]) << k;
+                out[dst] = label;
+            }
+    free(start);
+    return 0;
+}
+
+/* out[w,h,i,j] = round(round(scores[w,h,i,j] + bias[type(w),h,i,j]) + m)
+ * with m = 0 when rows i and j of window w carry the same region label and
+ * m = round(mask_value) otherwise; without labels (region == NULL, an
+ * unshifted block) out = round(scores + bias).  Two rounding points, as an
+ * eager "attn + bias; attn + mask" sequence in the tensor's format makes
+ * them; the mask is added to every element, zeros included (so -0 + 0
+ * gives +0).  scores/out [n_win, heads, n, n], bias [n_types, heads, n, n],
+ * win_type [n_win] (NULL: type 0), region [n_win * n]; fmt 0 = binary16,
+ * 1 = bfloat16. */
+void orc_window_bias_mask_add_fmt(const uint16_t *scores, const uint16_t *bias,
+                                  const int32_t *win_type, const int32_t *region, uint16_t *out,
+                                  int64_t n_win, int32_t heads, int32_t n, double mask_value,
+                                  int fmt)
+{
+    const double m = dec16(enc16(mask_value, fmt), fmt);
+    for (int64_t w = 0; w < n_win; ++w) {
+        const int64_t type = win_type ? win_type[w] : 0;
+        for (int32_t h = 0; h < heads; ++h)
+            for (int32_t i = 0; i < n; ++i)
+                for (int32_t j = 0; j < n; ++j) {
+                    const int64_t k = ((w * heads + h) * (int64_t)n + i) * n + j;
+                    const int64_t kb = ((type * heads + h) * (int64_t)n + i) * n + j;
+                    double t = dec16(enc16(dec16(scores[k], fmt) + dec16(bias[kb], fmt), fmt), fmt);
+                    if (region) {
+                        const int same = region[w * n + i] == region[w * n + j];
+                        t = dec16(enc16(t + (same ? 0.0 : m), fmt), fmt);
+                    }
+                    out[k] = enc16(t, fmt);
+                }
+    }
+}

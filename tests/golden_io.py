@@ -42,3 +42,21 @@ def gelu_tiny_input():
             elif parts[0] == "bias":
                 bias = vals
     return rows, bias
+
+
+def shift_region_cases():
+    """{name: dict(grid, win, shift, padded, flags, axes, windows={window_id: [labels]})}"""
+    cases = {}
+    with open(os.path.join(GOLDEN, "shift_regions_worked.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if parts[0] == "case":
+                cases[parts[1]] = dict(grid=_triple(parts[2]), win=_triple(parts[3]),
+                                       shift=_triple(parts[4]), padded=_triple(parts[5]),
+                                       flags=int(parts[6]), axes=int(parts[7]), windows={})
+            else:
+                cases[parts[0]]["windows"][int(parts[1])] = [int(v) for v in parts[2:]]
+    return cases

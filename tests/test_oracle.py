@@ -609,3 +609,151 @@ def test_gelu_backward_16_bit_rounding_points():
         exact_sum = ref.to(dt).double().sum(0)         # sum of the rounded gradients
         assert np.allclose(gb64, exact_sum.numpy(), rtol=1e-14, atol=1e-15)
         assert np.array_equal(gb, conv(exact_sum.to(dt)))
+
+
+# ------------------------------------------------------------ bias-mask ----
+
+from golden_io import shift_region_cases  # noqa: E402
+
+
+def _window_rows(P, win):
+    """Cells of every window in the destination order: [(window_id, [(z,h,w), ...])]."""
+    nwin = [-(-P[k] // win[k]) for k in range(3)]
+    out = []
+    for bz, bh, bw in itertools.product(*(range(m) for m in nwin)):
+        lo = (bz * win[0], bh * win[1], bw * win[2])
+        hi = [min(lo[k] + win[k], P[k]) for k in range(3)]
+        out.append(list(itertools.product(*(range(lo[k], hi[k]) for k in range(3)))))
+    return out
+
+
+@pytest.mark.parametrize("name", sorted(shift_region_cases()))
+def test_shift_regions_match_worked_fixture(name):
+    c = shift_region_cases()[name]
+    lab = oracle.build_shift_regions(c["grid"], c["win"], c["shift"], c["padded"], c["flags"],
+                                     c["axes"])
+    rows = _window_rows(c["padded"], c["win"])
+    assert lab.size == sum(len(r) for r in rows)
+    start = np.cumsum([0] + [len(r) for r in rows])
+    assert sorted(c["windows"]) == list(range(len(rows)))
+    for wid, want in c["windows"].items():
+        assert list(lab[start[wid]:start[wid + 1]]) == want, (name, wid)
+
+
+def _swin_slice_ids(P, win, shift):
+    """Region ids of the classic shifted-window mask: on the padded grid,
+    each axis is cut into [0, P-w), [P-w, P-s), [P-s, P) (one slice when
+    s = 0) and every cell gets the index of its slice triple."""
+    ids = np.zeros(P, dtype=np.int64)
+    cnt = 0
+    cuts = []
+    for k in range(3):
+        s = shift[k] % P[k]
+        cuts.append([slice(0, P[k] - win[k]), slice(P[k] - win[k], P[k] - s), slice(P[k] - s, P[k])]
+                    if s else [slice(0, P[k])])
+    for a in cuts[0]:
+        for b in cuts[1]:
+            for c in cuts[2]:
+                ids[a, b, c] = cnt
+                cnt += 1
+    return ids
+
+
+@pytest.mark.parametrize("grid,win,shift", [((4, 12, 24), (2, 6, 12), (1, 3, 6)),
+                                            ((3, 11, 20), (2, 6, 12), (1, 3, 6)),
+                                            ((2, 6, 8), (2, 3, 4), (1, 1, 2)),
+                                            ((4, 6, 6), (2, 3, 3), (1, 2, 1))])
+def test_shift_regions_partition_windows_like_the_classic_slice_mask(grid, win, shift):
+    # pad-then-shift on full windows is the classic construction's setting
+    P = [-(-grid[k] // win[k]) * win[k] for k in range(3)]
+    lab = oracle.build_shift_regions(grid, win, shift, None, 1, 7)
+    ids = _swin_slice_ids(P, win, shift)
+    d = 0
+    for cells in _window_rows(P, win):
+        ours = lab[d:d + len(cells)]
+        theirs = np.array([ids[c] for c in cells])
+        assert np.array_equal(ours[:, None] == ours[None, :], theirs[:, None] == theirs[None, :])
+        d += len(cells)
+    assert d == lab.size
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("axes", [7, 3, 4])
+def test_shift_regions_separate_exactly_the_rows_the_roll_cut_apart(flags, axes):
+    # Two tokens of a window share a region iff, along every masked axis,
+    # their source coordinates are as far apart as their cells (the roll
+    # put no seam between them).  Checked on real tokens through the index
+    # map, with no use of the label formula.
+    grid, win, shift = (3, 11, 20), (2, 6, 12), (1, 3, 6)
+    P = [-(-grid[k] // win[k]) * win[k] for k in range(3)]
+    idx = oracle.build_window_index(grid, win, shift, None, flags)
+    lab = oracle.build_shift_regions(grid, win, shift, None, flags, axes)
+    d = 0
+    for cells in _window_rows(P, win):
+        rows = [(c, idx[d + i], lab[d + i]) for i, c in enumerate(cells) if idx[d + i] >= 0]
+        for (c1, t1, l1), (c2, t2, l2) in itertools.combinations(rows, 2):
+            s1 = np.unravel_index(t1, grid)
+            s2 = np.unravel_index(t2, grid)
+            together = all(s2[k] - s1[k] == c2[k] - c1[k] for k in range(3) if (axes >> k) & 1)
+            assert (l1 == l2) == together, (c1, c2)
+        d += len(cells)
+
+
+def test_shift_regions_without_shift_are_one_region():
+    lab = oracle.build_shift_regions((4, 11, 20), (2, 6, 12), (0, 0, 0), None, 0, 7)
+    assert lab.size == 4 * 12 * 24 and not lab.any()
+
+
+def _torch_bias_mask(s, b, win_type, region, mask_value, tdtype):
+    """The eager sequence attn + bias; attn + mask in the tensor format."""
+    t = s + b[torch.as_tensor(win_type, dtype=torch.long)]
+    if region is None:
+        return t
+    r = torch.as_tensor(region).view(s.shape[0], 1, s.shape[2])
+    m = torch.where(r.transpose(1, 2) == r, torch.tensor(0.0), torch.tensor(float(mask_value)))
+    return t + m.to(tdtype).unsqueeze(1)
+
+
+def _as_np(t, fmt):
+    return t.numpy() if fmt == "f16" else t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("fmt,tdtype", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+@pytest.mark.parametrize("masked", [True, False])
+def test_bias_mask_add_matches_the_eager_torch_sequence(fmt, tdtype, masked):
+    n_win, heads, n, n_types = 6, 3, 24, 2
+    s, b = synth.attention_logits(n_win, heads, n, n_types, seed=11, dtype=tdtype)
+    s = s.clone()
+    flat = s.view(-1)
+    # special values: signed zeros, infinities, NaN, overflow, exact cancellation
+    big = 60000.0 if fmt == "f16" else 3.0e38
+    flat[:8] = torch.tensor([0.0, -0.0, float("inf"), -float("inf"), float("nan"), big, -big, 1.0],
+                            dtype=tdtype)
+    b.view(-1)[:8] = torch.tensor([-0.0, -0.0, 1.0, -1.0, 0.0, big, -big, -1.0], dtype=tdtype)
+    win_type = np.arange(n_win, dtype=np.int32) % n_types
+    region = (np.arange(n_win * n, dtype=np.int32) // 5) % 3 if masked else None
+    ours = oracle.window_bias_mask_add(_as_np(s, fmt), _as_np(b, fmt), win_type, region, -100.0,
+                                       fmt=fmt)
+    ref = _as_np(_torch_bias_mask(s, b, win_type, region, -100.0, tdtype), fmt)
+    dec = oracle.f16_to_f64 if fmt == "f16" else oracle.bf16_to_f64
+    o, r = dec(ours), dec(ref)
+    assert np.array_equal(np.isnan(o), np.isnan(r))
+    ok = ~np.isnan(o)
+    assert np.array_equal(o[ok], r[ok])
+    assert np.array_equal(np.signbit(o[ok]), np.signbit(r[ok]))   # -0 + 0 = +0 when masked
+
+
+def test_bias_mask_add_uses_the_window_type_and_both_rounding_points():
+    # a bias picked by row instead of window type, or one rounding instead
+    # of two, changes these values
+    s = np.array([[[[1.0, 2048.0], [0.5, -3.0]]]], dtype=np.float16)      # [1,1,2,2]
+    b = np.array([[[[0.0, 0.0], [0.0, 0.0]]], [[[0.25, 1.0], [0.0009765625, 0.5]]]],
+                 dtype=np.float16)                                       # [2,1,2,2]
+    out = oracle.window_bias_mask_add(s, b, np.array([1], np.int32), np.array([0, 1], np.int32),
+                                      -100.0)
+    # (1 + 0.25) -> 1.25; masked pair (0,1): 2048 + 1 -> 2048 (tie to even), then -100 -> 1948
+    # (1,0): 0.5 + 2^-10 = 0.5009765625, then -100 -> -99.5 (one rounding would give -99.5 too,
+    # so (1,1) checks the second point: -3 + 0.5 = -2.5 exactly, unmasked)
+    assert out.ravel().tolist() == [1.25, 1948.0, -99.5, -2.5]
+    one_round = np.float16(np.float64(2048.0) + 1.0 - 100.0)
+    assert one_round != np.float16(1948.0)

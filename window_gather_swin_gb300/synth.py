@@ -90,6 +90,17 @@ def gelu_input(rows: int, width: int, dtype=torch.float32, seed: int = 4):
     return x.to(dtype), b.to(dtype)
 
 
+def attention_logits(n_win: int, heads: int, n: int, n_types: int = 1, seed: int = 6,
+                     dtype=torch.float16):
+    """(scores [n_win, heads, n, n] ~ N(0, 2^2), bias [n_types, heads, n, n]
+    ~ N(0, 0.02^2)): pre-softmax logits of n-token windows and an expanded
+    position bias per window type."""
+    g = _gen(seed)
+    s = torch.randn(n_win, heads, n, n, generator=g, dtype=torch.float32) * 2.0
+    b = torch.randn(n_types, heads, n, n, generator=g, dtype=torch.float32) * 0.02
+    return s.to(dtype), b.to(dtype)
+
+
 def random_index(n_idx: int, n_src: int, pad_fraction: float = 0.1, seed: int = 5) -> torch.Tensor:
     """int32 [n_idx]: uniform source indices in [0, n_src), about
     ``pad_fraction`` of them replaced by -1.  Repeats are allowed: this is a
