@@ -123,8 +123,9 @@ def build_calls():
 
 
 def build_next_calls():
-    """The block-boundary fusions beyond the step (window reverse + residual
-    add + LN; residual add + norm1 + window gather), at both stages."""
+    """The rows beyond the step: the block-boundary fusions (window reverse +
+    residual add + LN; residual add + norm1 + window gather) at both stages,
+    the bfloat16 forms, the GELU backward and the attention bias-mask add."""
     import window_gather_swin_gb300 as wgs
     calls = []
     for st in (synth.STAGE_192, synth.STAGE_384):
@@ -183,6 +184,17 @@ def build_next_calls():
     calls.append(Call("bias_gelu_tanh", f"bf16 [{rows},{width}]", 4 * rows * width + 2 * width,
                       {"x": xg, "bias": bg}, {"y": ((rows, width), bf)},
                       lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]), None, rows))
+    # position bias + shift mask on the attention logits (algorithmic bytes:
+    # logits read and written, the bias slab and the labels read once)
+    for ast in (synth.ATTN_192, synth.ATTN_384):
+        s_, b_ = synth.attention_logits(ast.n_win, ast.heads, ast.n, 1, seed=6)
+        reg = wgs.build_shift_regions(ast.grid, synth.WINDOW, synth.SHIFT, ast.padded)
+        calls.append(Call(
+            "window_bias_mask_add", f"fp16 [{ast.n_win},{ast.heads},{ast.n},{ast.n}]",
+            4 * s_.numel() + 2 * b_.numel() + 4 * reg.numel(),
+            {"s": s_, "b": b_, "reg": reg}, {"out": (tuple(s_.shape), torch.float16)},
+            lambda i, o: wgs.window_bias_mask_add(i["s"], i["b"], None, i["reg"], out=o["out"]),
+            None, ast.n_win * ast.heads * ast.n))
     return calls
 
 
@@ -238,8 +250,10 @@ def ncu_traffic():
     return out
 
 
-KERNEL_SOURCES = {
+KERNEL_SOURCES = {  # first matching prefix wins
+    "bias_gelu_tanh_bwd": ["window_gather_swin_gb300/csrc/wgs_gelu_bwd.cu"],
     "bias_gelu_tanh": ["window_gather_swin_gb300/csrc/wgs_gelu.cu"],
+    "window_bias_mask_add": ["window_gather_swin_gb300/csrc/wgs_bias_mask.cu"],
     "": ["window_gather_swin_gb300/csrc/wgs_rows.cu"],  # LN, add + LN, gathers
 }
 

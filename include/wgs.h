@@ -31,8 +31,9 @@
  *   - fp16 is IEEE binary16; "fp16(v)" below is round-to-nearest-even.
  *   - The kernels run only on compute capability 10.3 (sm_103a); on any
  *     other device the entry points return WGS_ERR_ARCH.
- *   - Calls are thread-safe; the only shared state is the per-device index
- *     error word read by wgs_check_error().
+ *   - Calls are thread-safe; the shared state is the per-device index
+ *     error word read by wgs_check_error() (and the scratch array of
+ *     bias_gelu_tanh_bwd_noalloc).
  */
 #ifndef WGS_H
 #define WGS_H
@@ -279,6 +280,38 @@ wgs_status bias_gelu_tanh_bwd_noalloc(const void *grad_y, const void *x, const v
                                       wgs_dtype dtype, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* window_bias_mask_add -- position bias + shift mask before softmax    */
+/*                                                          [P1 s6, s7] */
+/* ------------------------------------------------------------------ */
+/* P1 s7 keeps a "bias-mask" op in the final combination and s6 rejects
+ * fusing it with softmax; the pages give no arithmetic.  This library's
+ * reading is the shifted-window transformer's general one: the attention
+ * logits of every window and head receive a position bias and, in shifted
+ * blocks, a mask between rows that the cyclic roll brought together:
+ *     t[w,h,i,j]   = fp(scores[w,h,i,j] + bias[type[w],h,i,j])
+ *     out[w,h,i,j] = fp(t + (region[w*n+i] == region[w*n+j] ? 0 : m))
+ * where fp() rounds to nearest-even in `dtype` and m = fp(mask_value); the
+ * mask term is added to every element (so -0 becomes +0 where it is 0).
+ * With region == NULL (an unshifted block) out = t.
+ *   scores, out  [n_win, heads, n, n] of dtype (WGS_F16 or WGS_BF16);
+ *                out may equal scores, other overlaps return WGS_ERR_ALIAS.
+ *   bias         [n_types, heads, n, n] of dtype: the position bias already
+ *                expanded from its table, one slab per window type.
+ *   win_type     int32 [n_win] in [0, n_types), or NULL for type 0 (then
+ *                n_types may be 1).  A type outside the range writes that
+ *                window's outputs as zeros and sets the device error word
+ *                (wgs_check_error); nothing faults.
+ *   region       int32 [n_win * n] labels (wgs_build_shift_regions), or NULL.
+ * n_win * heads * n must be below 2^31 (else WGS_ERR_SHAPE).  The 16-byte
+ * path needs n a multiple of 8 (n <= 2048), scores / bias / out 16-byte
+ * aligned and region 16-byte aligned; otherwise a scalar path runs (same
+ * results). */
+wgs_status window_bias_mask_add(const void *scores, const void *bias, const int32_t *win_type,
+                                const int32_t *region, void *out, int64_t n_win, int32_t heads,
+                                int32_t n, int32_t n_types, float mask_value, wgs_dtype dtype,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* Host-side window index map                                 [P1 s5] */
 /* ------------------------------------------------------------------ */
 /* The page fixes the protocol (INT32 per destination row, >= 0 source
@@ -318,10 +351,28 @@ wgs_status wgs_build_window_inverse(const int32_t grid[3], const int32_t window[
                                     const int32_t shift[3], const int32_t *padded, int32_t flags,
                                     int32_t *inv_host, int64_t out_len);
 
+/* Fill out_host[0 .. count) with the shift-mask region label of every
+ * windowed row, in the map's destination order (same arguments as
+ * wgs_build_window_index, plus axes_mask).  Along axis k (bit k of
+ * axes_mask set) a row's cell c holds the token rolled in from c + s_k of
+ * the roll's period (the grid for WGS_SHIFT_THEN_PAD, the padded grid for
+ * WGS_PAD_THEN_SHIFT, s_k the shift taken modulo that period); when s_k is
+ * not 0 the cell lies past the roll's seam if c + s_k >= period_k.  The
+ * label is the sum over masked axes of 2^k * [past the seam along k]; pad
+ * cells follow the same rule.  Two rows of a window share a label exactly
+ * when the roll put no seam between them along a masked axis, the regions
+ * of the classic shifted-window attention mask.  axes_mask = 7 masks every
+ * axis; a periodic axis (longitude) can be left out.  Host memory only;
+ * out_len must be at least the count, else WGS_ERR_SHAPE. */
+wgs_status wgs_build_shift_regions(const int32_t grid[3], const int32_t window[3],
+                                   const int32_t shift[3], const int32_t *padded, int32_t flags,
+                                   int32_t axes_mask, int32_t *out_host, int64_t out_len);
+
 /* Read and clear the current device's index error word after the work
  * already queued on `stream` has finished.  This call synchronises
  * `stream`.  Returns WGS_ERR_INDEX if any gather since the last check met
- * an index outside [-1, n_src), WGS_OK otherwise.  The word is shared by
+ * an index outside [-1, n_src), or any window_bias_mask_add a window type
+ * outside [0, n_types); WGS_OK otherwise.  The word is shared by
  * every stream of the device. */
 wgs_status wgs_check_error(cudaStream_t stream);
 

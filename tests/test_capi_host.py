@@ -240,3 +240,63 @@ def test_gelu_backward_argument_errors(lib):
     assert f(A, B, C, B + 64, A + 2 ** 24, W, need, 1000, 768, 0, None) == ALIAS   # grad_x in x
     assert f(A, B, C, D, C + 4, W, need, 1000, 768, 0, None) == ALIAS             # grad_bias in bias
     assert f(A, B, C, D, A + 2 ** 24, D + 64, need, 1000, 768, 0, None) == ALIAS  # workspace in grad_x
+
+
+# ------------------------------------------------------------ bias-mask ----
+
+REGION_CASES = [((8, 91, 180), (8, 96, 180), 0, 7), ((4, 91, 90), (4, 96, 96), 0, 7),
+                ((4, 91, 90), (4, 96, 96), 0, 3), ((3, 11, 20), None, 1, 7),
+                ((3, 11, 20), None, 0, 5), ((2, 12, 24), None, 0, 7)]
+
+
+@pytest.mark.parametrize("grid,padded,flags,axes", REGION_CASES)
+def test_library_shift_regions_equal_oracle(grid, padded, flags, axes):
+    ours = wgs.build_shift_regions(grid, synth.WINDOW, synth.SHIFT, padded, flags, axes).numpy()
+    want = oracle.build_shift_regions(grid, synth.WINDOW, synth.SHIFT, padded, flags, axes)
+    assert np.array_equal(ours, want)
+
+
+@pytest.mark.parametrize("shift", [(0, 0, 0), (-1, 5, 0), (3, -7, 25), (1, 1, 1)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_library_shift_regions_odd_shifts(shift, flags):
+    grid, win = (5, 13, 27), (2, 6, 12)
+    ours = wgs.build_shift_regions(grid, win, shift, None, flags, 7).numpy()
+    assert np.array_equal(ours, oracle.build_shift_regions(grid, win, shift, None, flags, 7))
+
+
+def test_shift_region_builder_errors(lib):
+    g, w, s = (ctypes.c_int32 * 3)(2, 12, 24), (ctypes.c_int32 * 3)(2, 6, 12), (ctypes.c_int32 * 3)(1, 3, 6)
+    out = (ctypes.c_int32 * 576)()
+    f = lib.wgs_build_shift_regions
+    assert f(g, w, s, None, 0, 7, out, 576) == OK
+    assert f(g, w, s, None, 0, 7, out, 575) == SHAPE
+    assert f(g, w, s, None, 2, 7, out, 576) == SHAPE
+    assert f(g, w, s, None, 0, 8, out, 576) == SHAPE
+    assert f(g, w, s, None, 0, -1, out, 576) == SHAPE
+    assert f(None, w, s, None, 0, 7, out, 576) == NULL
+    assert f(g, w, s, None, 0, 7, None, 576) == NULL
+    bad = (ctypes.c_int32 * 3)(2, 12, 20)
+    assert f(g, w, s, bad, 0, 7, out, 576) == SHAPE              # padded < grid
+
+
+def test_bias_mask_argument_errors(lib):
+    f = lib.window_bias_mask_add
+    R = 0x50000000
+    # (scores, bias, win_type, region, out, n_win, heads, n, n_types, mask, dtype, stream)
+    assert f(A, B, None, R, C, 4, 6, 144, 1, -100.0, 0, None) == DTYPE          # fp32
+    assert f(A, B, None, R, C, 4, 6, 144, 1, -100.0, 3, None) == DTYPE
+    assert f(A, B, None, R, C, -1, 6, 144, 1, -100.0, 1, None) == SHAPE
+    assert f(A, B, None, R, C, 4, 6, 144, -1, -100.0, 1, None) == SHAPE
+    assert f(None, None, None, None, None, 0, 6, 144, 1, -100.0, 1, None) == OK  # empty
+    assert f(None, None, None, None, None, 4, 0, 144, 0, -100.0, 1, None) == OK
+    assert f(A, B, None, R, C, 4, 6, 144, 0, -100.0, 1, None) == SHAPE          # no bias slab
+    assert f(A, B, None, R, C, 2 ** 31 // 144 + 1, 1, 144, 1, -100.0, 1, None) == SHAPE  # 2^31 rows
+    assert f(None, B, None, R, C, 4, 6, 144, 1, -100.0, 1, None) == NULL
+    assert f(A, None, None, R, C, 4, 6, 144, 1, -100.0, 2, None) == NULL
+    assert f(A, B, None, R, None, 4, 6, 144, 1, -100.0, 1, None) == NULL
+    assert f(A + 1, B, None, R, C, 4, 6, 144, 1, -100.0, 1, None) == ALIGN
+    assert f(A, B, None, R + 2, C, 4, 6, 144, 1, -100.0, 1, None) == ALIGN
+    assert f(A, B, R + 2, None, C, 4, 6, 144, 1, -100.0, 1, None) == ALIGN
+    assert f(A, B, None, R, A + 64, 4, 6, 144, 1, -100.0, 1, None) == ALIAS      # shifted out
+    assert f(A, B, None, R, B, 4, 6, 144, 1, -100.0, 1, None) == ALIAS           # out = bias
+    assert f(A, B, None, C + 16, C, 4, 6, 144, 1, -100.0, 1, None) == ALIAS      # region in out

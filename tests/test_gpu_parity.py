@@ -635,6 +635,9 @@ def test_identical_results_when_captured_in_a_cuda_graph():
     m = window_map(st).to(dev)
     inv = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT).to(dev)
     xl = synth.ln_input(777, 384, seed=9).to(dev)
+    sc, bb = synth.attention_logits(m.numel() // 144, 2, 144, 1, seed=4)
+    sc, bb = sc.to(dev), bb.to(dev)
+    reg = wgs.build_shift_regions(st.grid, synth.WINDOW, synth.SHIFT, st.padded).to(dev)
 
     def run(outs):
         wgs.residual_add_ln_fwd(a, b, EPS, residual_out=outs["r"], out=outs["y"])
@@ -645,6 +648,7 @@ def test_identical_results_when_captured_in_a_cuda_graph():
         wgs.residual_add_norm_gather(a, b, m, EPS, residual_out=outs["r2"], out=outs["g2"])
         wgs.window_reverse_add_ln_fwd(a, outs["w"], inv, EPS, residual_out=outs["r3"],
                                       out=outs["y3"])
+        wgs.window_bias_mask_add(sc, bb, None, reg, out=outs["s"])
 
     def fresh():
         return {"r2": torch.empty_like(a), "g2": torch.empty(m.numel(), 192, dtype=torch.float16,
@@ -653,7 +657,7 @@ def test_identical_results_when_captured_in_a_cuda_graph():
                 "r": torch.empty_like(a), "y": torch.empty_like(a),
                 "g": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
                 "w": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
-                "l": torch.empty_like(xl), "z": torch.empty_like(x)}
+                "l": torch.empty_like(xl), "z": torch.empty_like(x), "s": torch.empty_like(sc)}
 
     eager = fresh()
     run(eager)
@@ -670,3 +674,110 @@ def test_identical_results_when_captured_in_a_cuda_graph():
     torch.cuda.synchronize(dev)
     for k in eager:
         assert torch.equal(eager[k].view(torch.uint8), graphed[k].view(torch.uint8)), k
+
+
+# ------------------------------------------------------------ bias-mask ----
+
+def _nan16(bits, fmt):
+    e, m = (0x7C00, 0x03FF) if fmt == "f16" else (0x7F80, 0x007F)
+    return ((bits & e) == e) & ((bits & m) != 0)
+
+
+def _check_bias_mask(gpu, want, fmt, what):
+    """Bit-exact (both results are correctly rounded adds); NaN payloads may differ."""
+    g = _bits(gpu).ravel()
+    w = np.ascontiguousarray(want).view(np.uint16).ravel()
+    ng, nw = _nan16(g, fmt), _nan16(w, fmt)
+    assert np.array_equal(ng, nw), f"{what}: NaN positions differ"
+    bad = np.flatnonzero((g != w) & ~ng)
+    assert bad.size == 0, f"{what}: {bad.size} elements differ, first at {bad[:5].tolist()}"
+
+
+def _to_oracle(t, fmt):
+    return np_(t) if fmt == "f16" else _bits(t)
+
+
+def _bias_types(st, per_type):
+    if not per_type:
+        return None, 1
+    n_lon = st.padded[2] // synth.WINDOW[2]
+    return (np.arange(st.n_win, dtype=np.int32) // n_lon), st.z_h_windows
+
+
+@pytest.mark.parametrize("dtype,fmt", [(torch.float16, "f16"), (torch.bfloat16, "bf16")])
+@pytest.mark.parametrize("st,per_type,axes", [(synth.ATTN_192, False, 7), (synth.ATTN_384, False, 7),
+                                              (synth.ATTN_384, True, 3)],
+                         ids=["c192", "c384", "c384-typed-periodic"])
+def test_bias_mask_full_size(st, per_type, axes, dtype, fmt):
+    """The benchmark's workloads, every output element against the oracle."""
+    types, n_types = _bias_types(st, per_type)
+    s, b = synth.attention_logits(st.n_win, st.heads, st.n, n_types, seed=21, dtype=dtype)
+    reg = wgs.build_shift_regions(st.grid, synth.WINDOW, synth.SHIFT, st.padded, 0, axes)
+    wt = None if types is None else torch.from_numpy(types).to(DEV)
+    out = wgs.window_bias_mask_add(s.to(DEV), b.to(DEV), wt, reg.to(DEV), -100.0)
+    want = oracle.window_bias_mask_add(_to_oracle(s, fmt), _to_oracle(b, fmt), types, reg.numpy(),
+                                       -100.0, fmt=fmt)
+    _check_bias_mask(out, want, fmt, f"bias-mask {st.name} {fmt}")
+    wgs.check_error(DEV)
+
+
+@pytest.mark.parametrize("fmt,dtype", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+@pytest.mark.parametrize("n_win,heads,n", [(1, 1, 8), (5, 3, 16), (37, 2, 24), (3, 1, 2048),
+                                           (7, 2, 12), (2, 3, 6), (1, 1, 1)])
+@pytest.mark.parametrize("masked", [True, False])
+def test_bias_mask_sizes_and_paths(n_win, heads, n, masked, fmt, dtype):
+    """Vector path (n % 8 == 0) and scalar path, ragged row blocks, window
+    types, labels and in-place use."""
+    rng = np.random.default_rng(n_win * 1000 + n)
+    n_types = 3
+    s, b = synth.attention_logits(n_win, heads, n, n_types, seed=n + heads, dtype=dtype)
+    types = rng.integers(0, n_types, n_win).astype(np.int32)
+    reg = rng.integers(0, 4, n_win * n).astype(np.int32) if masked else None
+    want = oracle.window_bias_mask_add(_to_oracle(s, fmt), _to_oracle(b, fmt), types, reg, -37.5,
+                                       fmt=fmt)
+    sd = s.to(DEV)
+    args = (b.to(DEV), torch.from_numpy(types).to(DEV),
+            None if reg is None else torch.from_numpy(reg).to(DEV), -37.5)
+    _check_bias_mask(wgs.window_bias_mask_add(sd, *args), want, fmt, "out of place")
+    wgs.window_bias_mask_add(sd, *args, out=sd)
+    _check_bias_mask(sd, want, fmt, "in place")
+    wgs.check_error(DEV)
+
+
+def test_bias_mask_misaligned_views_and_specials():
+    """A 2-byte-offset view takes the scalar path; signed zeros, infinities,
+    NaN and overflow give the oracle's bits on both paths."""
+    n_win, heads, n = 6, 2, 16
+    s, b = synth.attention_logits(n_win, heads, n, 1, seed=5)
+    flat = s.view(-1)
+    flat[:10] = torch.tensor([0.0, -0.0, float("inf"), -float("inf"), float("nan"), 60000.0,
+                              -60000.0, 65504.0, -0.0, 1.0], dtype=torch.float16)
+    b.view(-1)[:10] = torch.tensor([-0.0, -0.0, 1.0, -1.0, 0.0, 60000.0, -60000.0, 32.0, 0.0,
+                                    -1.0], dtype=torch.float16)
+    reg = (np.arange(n_win * n, dtype=np.int32) * 7) % 3
+    want = oracle.window_bias_mask_add(np_(s), np_(b), None, reg, -100.0)
+    regd = torch.from_numpy(reg).to(DEV)
+    _check_bias_mask(wgs.window_bias_mask_add(s.to(DEV), b.to(DEV), None, regd), want, "f16",
+                     "aligned")
+    buf = torch.empty(s.numel() + 1, dtype=torch.float16, device=DEV)
+    view = buf[1:].view(s.shape)
+    view.copy_(s.to(DEV))
+    assert view.data_ptr() % 16 != 0
+    _check_bias_mask(wgs.window_bias_mask_add(view, b.to(DEV), None, regd), want, "f16",
+                     "misaligned")
+    wgs.check_error(DEV)
+
+
+def test_bias_mask_bad_window_type_sets_error_word():
+    n_win, heads, n = 4, 2, 16
+    s, b = synth.attention_logits(n_win, heads, n, 2, seed=8)
+    types = np.array([0, 1, 2, -1], dtype=np.int32)           # windows 2 and 3 out of range
+    out = wgs.window_bias_mask_add(s.to(DEV), b.to(DEV), torch.from_numpy(types).to(DEV))
+    with pytest.raises(wgs.WgsError) as e:
+        wgs.check_error(DEV)
+    assert e.value.status == 8                                   # WGS_ERR_INDEX
+    o = np_(out)
+    assert not o[2:].any() and not np.signbit(o[2:]).any()      # +0 rows
+    want = oracle.window_bias_mask_add(np_(s)[:2], np_(b), types[:2], None)
+    _check_bias_mask(out[:2], want, "f16", "good windows")
+    wgs.check_error(DEV)                                         # cleared

@@ -44,6 +44,8 @@ SIGNATURES = {
     "bias_gelu_tanh_bwd_noalloc": (_st, [_P, _P, _P, _P, _P, _i64, _i32, _i32, _P]),
     "wgs_window_index_count": (_i64, [_P, _P, _P]),
     "wgs_build_window_index": (_st, [_P, _P, _P, _P, _i32, _P, _i64]),
+    "window_bias_mask_add": (_st, [_P, _P, _P, _P, _P, _i64, _i32, _i32, _i32, _f32, _i32, _P]),
+    "wgs_build_shift_regions": (_st, [_P, _P, _P, _P, _i32, _i32, _P, _i64]),
     "wgs_check_error": (_st, [_P]),
 }
 

@@ -252,6 +252,40 @@ def bias_gelu_tanh_bwd(grad_y: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
     return gx, gb
 
 
+def window_bias_mask_add(scores: torch.Tensor, bias: torch.Tensor,
+                         win_type: Optional[torch.Tensor] = None,
+                         region: Optional[torch.Tensor] = None, mask_value: float = -100.0,
+                         out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention logits plus position bias and shift mask: scores
+    [n_win, heads, n, n] (float16 or bfloat16), bias [n_types, heads, n, n],
+    win_type int32 [n_win] (None: type 0), region int32 [n_win * n] labels
+    (None: no mask).  out may be scores."""
+    _row16(scores, "scores")
+    _cuda(bias, "bias", scores.dtype)
+    _require(scores.dim() == 4 and scores.shape[2] == scores.shape[3],
+             f"scores must be [n_win, heads, n, n] (got {tuple(scores.shape)})")
+    n_win, heads, n, _ = scores.shape
+    _require(bias.dim() == 4 and tuple(bias.shape[1:]) == (heads, n, n),
+             f"bias must be [n_types, {heads}, {n}, {n}] (got {tuple(bias.shape)})")
+    n_types = bias.shape[0]
+    ts = [scores, bias]
+    if win_type is not None:
+        _cuda(win_type, "win_type", torch.int32)
+        _require(win_type.numel() == n_win, f"win_type must have {n_win} entries")
+        ts.append(win_type)
+    if region is not None:
+        _cuda(region, "region", torch.int32)
+        _require(region.numel() == n_win * n, f"region must have {n_win * n} entries")
+        ts.append(region)
+    y = _out(out, scores.shape, scores.dtype, scores.device, "out")
+    _same_device(*ts, y)
+    with torch.cuda.device(scores.device):
+        _capi.check("window_bias_mask_add", _capi.load().window_bias_mask_add(
+            _ptr(scores), _ptr(bias), _ptr(win_type), _ptr(region), _ptr(y), n_win, heads, n,
+            n_types, float(mask_value), _DTYPE[scores.dtype], _stream_ptr(scores.device)))
+    return y
+
+
 # ----------------------------------------------------------- index map ----
 
 SHIFT_THEN_PAD, PAD_THEN_SHIFT = 0, 1
@@ -299,9 +333,24 @@ def build_window_inverse(grid: Sequence[int], window: Sequence[int], shift: Sequ
     return out if device is None else out.to(device)
 
 
+def build_shift_regions(grid: Sequence[int], window: Sequence[int], shift: Sequence[int],
+                        padded: Optional[Sequence[int]] = None, flags: int = SHIFT_THEN_PAD,
+                        axes_mask: int = 7, device=None) -> torch.Tensor:
+    """INT32 shift-mask region label per windowed row (host-built), in the
+    index map's order; on `device` if given."""
+    n = window_index_count(grid, window, padded)
+    out = torch.empty(n, dtype=torch.int32)
+    _capi.check("wgs_build_shift_regions", _capi.load().wgs_build_shift_regions(
+        _i3(grid, "grid"), _i3(window, "window"), _i3(shift, "shift"),
+        _i3(padded, "padded") if padded is not None else None, int(flags), int(axes_mask),
+        ctypes.c_void_p(out.data_ptr()), n))
+    return out if device is None else out.to(device)
+
+
 def check_error(device=None) -> None:
-    """Raise if any gather on `device` met an index outside [-1, n_src)
-    since the last check.  Synchronises that device's current stream."""
+    """Raise if any gather on `device` met an index outside [-1, n_src), or
+    any bias-mask add a window type outside [0, n_types), since the last
+    check.  Synchronises that device's current stream."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     with torch.cuda.device(dev):
         _capi.check("wgs_check_error", _capi.load().wgs_check_error(_stream_ptr(dev)))

@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libwgs.so")
 
-SOURCES = ["wgs_rows.cu", "wgs_gelu.cu", "wgs_gelu_bwd.cu", "wgs_runtime.cu", "wgs_index.cpp"]
+SOURCES = ["wgs_rows.cu", "wgs_gelu.cu", "wgs_gelu_bwd.cu", "wgs_bias_mask.cu", "wgs_runtime.cu",
+           "wgs_index.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,241 @@
+// Position bias + shift mask added to the pre-softmax attention logits of a
+// shifted-window transformer (sm_103a).
+//
+// Page "BW1000 gfx936 Pangu-Weather inference profiling", s7 keeps a
+// "bias-mask" op in the final combination and s6 rejects fusing it with
+// softmax; the pages do not give its arithmetic.  The reading here is the
+// shifted-window transformer's general one, with the rounding points of an
+// eager "attn + bias; attn + mask" sequence in the tensor's format:
+//     t   = fp(scores[w,h,i,j] + bias[type[w],h,i,j])
+//     out = fp(t + (region[w,i] == region[w,j] ? 0 : m))      (region given)
+// The logits tensor is streamed once (read, written); the bias slabs
+// (n_types x heads x n x n, a few hundred KB per type) and the region labels
+// are re-read by every window and stay in L2 / L1.
+//
+// Layout: a logits row is n 16-bit elements = n/8 16-byte chunks.  A CTA of
+// RP x (n/8) threads gives every thread one fixed chunk column and RP rows
+// per pass, U passes in flight; the grid strides over blocks of RP x U rows
+// of the flattened [n_win x heads x n] row space.  A row's window, head and
+// query index come from two divisions by invariant integers done as
+// multiply-high (Granlund & Montgomery 1994).
+#include <atomic>
+
+#include "wgs_common.cuh"
+
+#ifndef WGS_BM_U
+#define WGS_BM_U 2  // rows in flight per thread
+#endif
+#ifndef WGS_BM_THREADS
+#define WGS_BM_THREADS 128  // most threads per CTA (vector path)
+#endif
+
+namespace wgs {
+
+namespace {
+
+// x / d for 0 <= x < 2^31 and 1 <= d < 2^31 with one multiply-high
+// (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", 1994, s4): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, x / d = (mulhi(x, m) + x) >> l.  The
+// sum stays below 2^32 because mulhi(x, m) <= x < 2^31.
+struct FastDiv {
+    uint32_t m, l;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t{1} << l) < d) ++l;
+    const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+    return {static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ uint32_t div_by(uint32_t x, FastDiv f) {
+    return (__umulhi(x, f.m) + x) >> f.l;
+}
+
+// The mask term of one 32-bit word (two elements): m in each half whose
+// column label differs from the row label, +0 elsewhere.
+__device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t c_hi,
+                                              uint32_t mask2) {
+    return (c_lo != row ? (mask2 & 0xffffu) : 0u) | (c_hi != row ? (mask2 & 0xffff0000u) : 0u);
+}
+
+template <typename E, int U>
+__global__ void __launch_bounds__(WGS_BM_THREADS)
+bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
+              const int32_t *region, uint4 *out, unsigned int *err, uint32_t rows, int32_t n,
+              int32_t heads, int32_t n_types, int32_t cpr, int32_t rp, FastDiv by_n,
+              FastDiv by_heads, uint32_t mask2) {
+    pdl_prologue();
+    const int jc = static_cast<int>(threadIdx.x) % cpr, lr = static_cast<int>(threadIdx.x) / cpr;
+    if (lr >= rp) return;  // no barrier below, so spare threads may leave
+    const uint32_t block = static_cast<uint32_t>(rp) * U;
+    for (uint32_t base = blockIdx.x * block; base < rows; base += gridDim.x * block) {
+        uint4 sv[U], bv[U];
+        int4 c0[U], c1[U];
+        int32_t li[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t r = base + lr + u * rp;
+            ok[u] = false;
+            if (r < rows) {
+                const uint32_t tile = div_by(r, by_n), i = r - tile * n;
+                const uint32_t w = div_by(tile, by_heads), h = tile - w * heads;
+                const int32_t type = win_type ? __ldg(win_type + w) : 0;
+                ok[u] = type >= 0 && type < n_types;
+                sv[u] = ld_stream(scores + static_cast<int64_t>(r) * cpr + jc);
+                if (ok[u])
+                    bv[u] = __ldg(bias + ((static_cast<int64_t>(type) * heads + h) * n + i) * cpr + jc);
+                if (region) {
+                    const int32_t *lab = region + static_cast<int64_t>(w) * n;
+                    li[u] = __ldg(lab + i);
+                    c0[u] = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc);
+                    c1[u] = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc + 1);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t r = base + lr + u * rp;
+            if (r >= rows) continue;
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (ok[u]) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t t = E::add2(word(sv[u], k), word(bv[u], k));
+                    if (region) {
+                        const int4 &c = k < 2 ? c0[u] : c1[u];
+                        const int32_t lo = (k & 1) ? c.z : c.x, hi = (k & 1) ? c.w : c.y;
+                        t = E::add2(t, mask_word(li[u], lo, hi, mask2));
+                    }
+                    set_word(o, k, t);
+                }
+            } else {
+                atomicOr(err, 1u);
+            }
+            st_stream(out + static_cast<int64_t>(r) * cpr + jc, o);
+        }
+    }
+}
+
+// Any n or alignment: one element per thread per step.
+template <typename E>
+__global__ void __launch_bounds__(256)
+bias_mask_scalar(const uint16_t *scores, const uint16_t *bias, const int32_t *win_type,
+                 const int32_t *region, uint16_t *out, unsigned int *err, int64_t total, int32_t n,
+                 int32_t heads, int32_t n_types, uint32_t mask2) {
+    pdl_prologue();
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = e / n, tile = r / n, w = tile / heads;
+        const int32_t j = static_cast<int32_t>(e - r * n), i = static_cast<int32_t>(r - tile * n);
+        const int32_t h = static_cast<int32_t>(tile - w * heads);
+        const int32_t type = win_type ? win_type[w] : 0;
+        uint16_t o = 0;
+        if (type >= 0 && type < n_types) {
+            uint32_t t = E::add2(scores[e], bias[((type * static_cast<int64_t>(heads) + h) * n + i) * n + j]);
+            if (region) {
+                const int32_t *lab = region + w * n;
+                t = E::add2(t, lab[i] != lab[j] ? (mask2 & 0xffffu) : 0u);
+            }
+            o = static_cast<uint16_t>(t);
+        } else {
+            atomicOr(err, 1u);
+        }
+        out[e] = o;
+    }
+}
+
+template <typename E>
+wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t *win_type,
+                            const int32_t *region, void *out, unsigned int *err, int64_t n_win,
+                            int32_t heads, int32_t n, int32_t n_types, uint32_t mask2,
+                            const DeviceInfo &dev, cudaStream_t stream) {
+    const int64_t rows = n_win * heads * n;
+    const int32_t cpr = n / 8;
+    const bool vec = n % 8 == 0 && cpr <= WGS_BM_THREADS && aligned16(scores) && aligned16(bias) &&
+                     aligned16(out) && (!region || aligned16(region));
+    if (vec) {
+        constexpr int U = WGS_BM_U;
+        const int32_t rp = WGS_BM_THREADS / cpr;
+        auto kernel = bias_mask_vec<E, U>;
+        static std::atomic<int> resident[64];  // per device, for this instantiation
+        int per_sm = resident[dev.device].load(std::memory_order_relaxed);
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, rp * cpr, 0) !=
+                    cudaSuccess ||
+                per_sm < 1)
+                return WGS_ERR_LAUNCH;
+            resident[dev.device].store(per_sm, std::memory_order_relaxed);
+        }
+        const int64_t blocks = ceil_div(rows, static_cast<int64_t>(rp) * U);
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
+        return launch(kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)),
+                      dim3(static_cast<unsigned>(rp * cpr)), 0, stream,
+                      static_cast<const uint4 *>(scores), static_cast<const uint4 *>(bias),
+                      win_type, region, static_cast<uint4 *>(out), err,
+                      static_cast<uint32_t>(rows), n, heads, n_types, cpr, rp,
+                      make_fastdiv(static_cast<uint32_t>(n)),
+                      make_fastdiv(static_cast<uint32_t>(heads)), mask2);
+    }
+    const int64_t total = rows * n;
+    const int64_t need = ceil_div(total, 256);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    return launch(bias_mask_scalar<E>, dim3(static_cast<unsigned>(need < cap ? need : cap)),
+                  dim3(256), 0, stream, static_cast<const uint16_t *>(scores),
+                  static_cast<const uint16_t *>(bias), win_type, region,
+                  static_cast<uint16_t *>(out), err, total, n, heads, n_types, mask2);
+}
+
+}  // namespace
+
+}  // namespace wgs
+
+using namespace wgs;
+
+extern "C" wgs_status window_bias_mask_add(const void *scores, const void *bias,
+                                           const int32_t *win_type, const int32_t *region,
+                                           void *out, int64_t n_win, int32_t heads, int32_t n,
+                                           int32_t n_types, float mask_value, wgs_dtype dtype,
+                                           cudaStream_t stream) {
+    if (dtype != WGS_F16 && dtype != WGS_BF16) return WGS_ERR_DTYPE;
+    if (n_win < 0 || heads < 0 || n < 0 || n_types < 0) return WGS_ERR_SHAPE;
+    if (n_win == 0 || heads == 0 || n == 0) return WGS_OK;
+    if (n_types < 1) return WGS_ERR_SHAPE;
+    if (n_win > (int64_t{1} << 31) / heads / n ||
+        n_win * heads * n >= (int64_t{1} << 31))
+        return WGS_ERR_SHAPE;
+    if (!scores || !bias || !out) return WGS_ERR_NULL;
+    if (((reinterpret_cast<uintptr_t>(scores) | reinterpret_cast<uintptr_t>(bias) |
+          reinterpret_cast<uintptr_t>(out)) & 1u) ||
+        !aligned4(win_type) || !aligned4(region))
+        return WGS_ERR_ALIGN;
+    const int64_t nn = static_cast<int64_t>(n) * n;
+    const int64_t bytes = n_win * heads * nn * 2, bbytes = static_cast<int64_t>(n_types) * heads * nn * 2;
+    if (!same_or_disjoint(out, scores, bytes) || overlap(out, bytes, bias, bbytes) ||
+        (win_type && overlap(out, bytes, win_type, n_win * 4)) ||
+        (region && overlap(out, bytes, region, n_win * n * 4)))
+        return WGS_ERR_ALIAS;
+    DeviceInfo dev;
+    wgs_status st = current_device(&dev);
+    if (st != WGS_OK) return st;
+    unsigned int *err = nullptr;
+    st = index_error_word(dev.device, &err);
+    if (st != WGS_OK) return st;
+    // the mask value rounded once to the tensor's format, in both halves
+    uint16_t m16;
+    if (dtype == WGS_F16) {
+        const __half h = __float2half_rn(mask_value);
+        memcpy(&m16, &h, 2);
+    } else {
+        const __nv_bfloat16 h = __float2bfloat16_rn(mask_value);
+        memcpy(&m16, &h, 2);
+    }
+    const uint32_t mask2 = static_cast<uint32_t>(m16) | (static_cast<uint32_t>(m16) << 16);
+    if (dtype == WGS_F16)
+        return launch_bias_mask<Fp16>(scores, bias, win_type, region, out, err, n_win, heads, n,
+                                      n_types, mask2, dev, stream);
+    return launch_bias_mask<Bf16>(scores, bias, win_type, region, out, err, n_win, heads, n,
+                                  n_types, mask2, dev, stream);
+}

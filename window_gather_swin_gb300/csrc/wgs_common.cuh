@@ -28,6 +28,11 @@ struct DeviceInfo {
 };
 wgs_status current_device(DeviceInfo *info);
 
+// Device address of the index error word (read by wgs_check_error) on
+// `device`, which must be current; for kernels of other translation units.
+// Looked up on the first call per device.
+wgs_status index_error_word(int device, unsigned int **out);
+
 // Launch `kernel` on `stream`.  With WGS_PDL the launch allows programmatic
 // dependent launch: the grid may be scheduled while the previous kernel on
 // the stream drains, and every kernel of this library starts with

@@ -127,3 +127,40 @@ extern "C" wgs_status wgs_build_window_inverse(const int32_t grid[3], const int3
             }
     return WGS_OK;
 }
+
+// Shift-mask region labels in the destination order of the map above: the
+// same window walk, with each cell labelled by the axes along which it lies
+// past the roll's seam.
+extern "C" wgs_status wgs_build_shift_regions(const int32_t grid[3], const int32_t window[3],
+                                              const int32_t shift[3], const int32_t *padded,
+                                              int32_t flags, int32_t axes_mask, int32_t *out_host,
+                                              int64_t out_len) {
+    if (!grid || !window || !shift || !out_host) return WGS_ERR_NULL;
+    if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
+    if (axes_mask < 0 || axes_mask > 7) return WGS_ERR_SHAPE;
+    int64_t ext[3];
+    if (!padded_extents(grid, window, padded, ext)) return WGS_ERR_SHAPE;
+    if (out_len < ext[0] * ext[1] * ext[2]) return WGS_ERR_SHAPE;
+    // seam[k]: first cell past the seam along k (ext[k] when the axis is
+    // not masked or not moved, so no cell is past it)
+    int64_t seam[3];
+    for (int k = 0; k < 3; ++k) {
+        const int64_t period = flags == WGS_PAD_THEN_SHIFT ? ext[k] : grid[k];
+        const int64_t s = wrap(shift[k], period);
+        seam[k] = ((axes_mask >> k) & 1) && s != 0 ? period - s : ext[k];
+    }
+    int64_t d = 0;
+    for (int64_t z0 = 0; z0 < ext[0]; z0 += window[0])
+        for (int64_t h0 = 0; h0 < ext[1]; h0 += window[1])
+            for (int64_t w0 = 0; w0 < ext[2]; w0 += window[2]) {
+                const int64_t z1 = z0 + window[0] < ext[0] ? z0 + window[0] : ext[0];
+                const int64_t h1 = h0 + window[1] < ext[1] ? h0 + window[1] : ext[1];
+                const int64_t w1 = w0 + window[2] < ext[2] ? w0 + window[2] : ext[2];
+                for (int64_t z = z0; z < z1; ++z)
+                    for (int64_t h = h0; h < h1; ++h)
+                        for (int64_t w = w0; w < w1; ++w)
+                            out_host[d++] = (z >= seam[0] ? 1 : 0) | (h >= seam[1] ? 2 : 0) |
+                                            (w >= seam[2] ? 4 : 0);
+            }
+    return WGS_OK;
+}

@@ -15,6 +15,8 @@
 // store; the statistics use the shifted-data two-pass method (see
 // ln_normalize).  Each warp works on U row groups at once so that every lane has
 // U * CPL independent 16-byte loads in flight before its first reduction.
+#include <atomic>
+
 #include "wgs_common.cuh"
 
 #ifndef WGS_ROW_WARPS
@@ -30,8 +32,29 @@
 namespace wgs {
 
 // Set (never cleared by a kernel) when a gather meets an index outside
-// [-1, n_src); read and cleared by wgs_check_error().
+// [-1, n_src), or the bias-mask add a window type outside its range; read
+// and cleared by wgs_check_error().
 __device__ unsigned int g_index_error;
+
+namespace {
+std::atomic<unsigned int *> g_index_error_ptr[64];
+}  // namespace
+
+wgs_status index_error_word(int device, unsigned int **out) {
+    if (device < 0 || device >= 64) return WGS_ERR_CUDA;
+    unsigned int *p = g_index_error_ptr[device].load(std::memory_order_acquire);
+    if (!p) {
+        void *q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_index_error) != cudaSuccess || !q) {
+            cudaGetLastError();  // clear this thread's error
+            return WGS_ERR_CUDA;
+        }
+        p = static_cast<unsigned int *>(q);
+        g_index_error_ptr[device].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return WGS_OK;
+}
 
 // kLN            y[r] = LN(x[r])
 // kAddLN         o[r] = fp16(a[r] + b[r]),         y[r] = LN(o[r])

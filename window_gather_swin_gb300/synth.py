@@ -48,6 +48,34 @@ TINY = Stage("tiny", (2, 12, 24), 192, (2, 12, 24))
 TINY_PADDED = Stage("tiny_padded", (3, 11, 20), 192, (4, 12, 24))
 STAGES = {s.name: s for s in (STAGE_192, STAGE_384, TINY, TINY_PADDED)}
 
+# Attention over uniform windows (window-major rows, as the index map lays
+# them out): the 192 stage's padded grid, and the 384 stage padded to whole
+# windows (4 x 96 x 96) since a batched attention needs equal windows.
+# Heads = width / 32.
+@dataclass(frozen=True)
+class AttnStage:
+    name: str
+    grid: tuple
+    padded: tuple
+    heads: int
+
+    @property
+    def n(self) -> int:
+        return WINDOW[0] * WINDOW[1] * WINDOW[2]
+
+    @property
+    def n_win(self) -> int:
+        return (self.padded[0] * self.padded[1] * self.padded[2]) // self.n
+
+    @property
+    def z_h_windows(self) -> int:
+        """Windows per longitude band: one position-bias type each."""
+        return (self.padded[0] // WINDOW[0]) * (self.padded[1] // WINDOW[1])
+
+
+ATTN_192 = AttnStage("c192", (8, 91, 180), (8, 96, 180), 6)
+ATTN_384 = AttnStage("c384", (4, 91, 90), (4, 96, 96), 12)
+
 # MLP hidden width is 4x the stage width.
 GELU_F32_SHAPE = (131040, 768)
 GELU_F16_SHAPE = (32760, 1536)
