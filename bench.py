@@ -591,7 +591,10 @@ def smi_id(dev):
 def run_e2e(calls, dev, args, world):
     """Same metric through the public API from pinned HOST buffers: every
     step copies each call's inputs host->device, runs it, and copies its
-    outputs device->host, all inside the timed region."""
+    outputs device->host, all inside the timed region.  Copies in, kernels
+    and copies out run on three streams, so call j's kernel overlaps call
+    j+1's upload and call j-1's download (the host link is full duplex);
+    events keep each buffer's uses in order across steps."""
     host_in = [{k: v.pin_memory() for k, v in c.inputs.items()} for c in calls]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in c.inputs.items()} for c in calls]
     dev_out = [{k: torch.empty(s, dtype=d, device=dev) for k, (s, d) in c.outputs.items()}
@@ -600,32 +603,66 @@ def run_e2e(calls, dev, args, world):
                 for c in calls]
     h2d = sum(v.numel() * v.element_size() for d in host_in for v in d.values())
     d2h = sum(v.numel() * v.element_size() for d in host_out for v in d.values())
-    stream = torch.cuda.current_stream(dev)
+    main = torch.cuda.current_stream(dev)
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    n = len(calls)
+    ev_in, ev_run, ev_out = ([torch.cuda.Event() for _ in range(n)] for _ in range(3))
+    for e in ev_run + ev_out:
+        e.record(main)
 
     def step():
-        for c, hi, di, do, ho in zip(calls, host_in, dev_in, dev_out, host_out):
-            for k in hi:
-                di[k].copy_(hi[k], non_blocking=True)
-            c.run(di, do)
-            for k in do:
-                ho[k].copy_(do[k], non_blocking=True)
+        for j, (c, hi, di, do, ho) in enumerate(zip(calls, host_in, dev_in, dev_out, host_out)):
+            s_in.wait_event(ev_run[j])          # the previous step's kernel has read di
+            with torch.cuda.stream(s_in):
+                for k in hi:
+                    di[k].copy_(hi[k], non_blocking=True)
+            ev_in[j].record(s_in)
+            s_run.wait_event(ev_in[j])
+            s_run.wait_event(ev_out[j])         # the previous step's download has read do
+            with torch.cuda.stream(s_run):
+                c.run(di, do)
+            ev_run[j].record(s_run)
+            s_out.wait_event(ev_run[j])
+            with torch.cuda.stream(s_out):
+                for k in do:
+                    ho[k].copy_(do[k], non_blocking=True)
+            ev_out[j].record(s_out)
+
+    def join():
+        for st in (s_in, s_run, s_out):
+            main.wait_stream(st)
 
     steps = max(1, min(args.steps, args.e2e_steps))
     for _ in range(max(1, min(args.warmup, 3))):
         step()
+    join()
     torch.cuda.synchronize(dev)
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(main)
+    for st in (s_in, s_run, s_out):
+        st.wait_stream(main)
     for _ in range(steps):
         step()
-    b.record(stream)
+    join()
+    b.record(main)
     torch.cuda.synchronize(dev)
     ms = reduce_max(a.elapsed_time(b), world, dev)
     total = reduce_sum(sum(c.bytes for c in calls) * steps, world, dev)
+    # the link alone, for context: one step's uploads, then its downloads
+    link = {}
+    for name, pairs in (("h2d_gbs", [(di[k], hi[k]) for hi, di in zip(host_in, dev_in) for k in hi]),
+                        ("d2h_gbs", [(ho[k], do[k]) for do, ho in zip(dev_out, host_out) for k in do])):
+        x, y = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x.record(main)
+        for dst, src in pairs:
+            dst.copy_(src, non_blocking=True)
+        y.record(main)
+        torch.cuda.synchronize(dev)
+        link[name] = round((h2d if name == "h2d_gbs" else d2h) / (x.elapsed_time(y) / 1e3) / 1e9, 1)
     return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "ms_per_step": round(ms / steps, 4)}
+            "ms_per_step": round(ms / steps, 4), "link_alone": link}
 
 
 # ------------------------------------------------------- reference arm ----

@@ -26,12 +26,16 @@
 #define WGS_BM_U 2  // rows in flight per thread
 #endif
 #ifndef WGS_BM_THREADS
-#define WGS_BM_THREADS 128  // most threads per CTA (vector path)
+#define WGS_BM_THREADS 128  // threads per CTA to aim for (vector path)
 #endif
 
 namespace wgs {
 
 namespace {
+
+// Vector-path CTAs: RP = max(1, WGS_BM_THREADS / (n/8)) rows of n/8 threads,
+// so at most 256 threads for the widest row the path takes (n = 2048).
+constexpr int kMaxChunksPerRow = 256;
 
 // x / d for 0 <= x < 2^31 and 1 <= d < 2^31 with one multiply-high
 // (Granlund & Montgomery, "Division by invariant integers using
@@ -61,7 +65,7 @@ __device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t
 }
 
 template <typename E, int U>
-__global__ void __launch_bounds__(WGS_BM_THREADS)
+__global__ void __launch_bounds__(kMaxChunksPerRow > WGS_BM_THREADS ? kMaxChunksPerRow : WGS_BM_THREADS)
 bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
               const int32_t *region, uint4 *out, unsigned int *err, uint32_t rows, int32_t n,
               int32_t heads, int32_t n_types, int32_t cpr, int32_t rp, FastDiv by_n,
@@ -154,20 +158,25 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
                             const DeviceInfo &dev, cudaStream_t stream) {
     const int64_t rows = n_win * heads * n;
     const int32_t cpr = n / 8;
-    const bool vec = n % 8 == 0 && cpr <= WGS_BM_THREADS && aligned16(scores) && aligned16(bias) &&
-                     aligned16(out) && (!region || aligned16(region));
+    const bool vec = n % 8 == 0 && cpr <= kMaxChunksPerRow && aligned16(scores) &&
+                     aligned16(bias) && aligned16(out) && (!region || aligned16(region));
     if (vec) {
         constexpr int U = WGS_BM_U;
-        const int32_t rp = WGS_BM_THREADS / cpr;
+        const int32_t rp = cpr < WGS_BM_THREADS ? WGS_BM_THREADS / cpr : 1;
         auto kernel = bias_mask_vec<E, U>;
-        static std::atomic<int> resident[64];  // per device, for this instantiation
-        int per_sm = resident[dev.device].load(std::memory_order_relaxed);
-        if (per_sm == 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, rp * cpr, 0) !=
+        // resident CTAs per SM for this CTA size, cached per device as
+        // (threads << 32 | CTAs)
+        static std::atomic<int64_t> resident[64];
+        const int threads = rp * cpr;
+        int64_t cached = resident[dev.device].load(std::memory_order_relaxed);
+        int per_sm = static_cast<int>(cached & 0xffffffff);
+        if ((cached >> 32) != threads || per_sm < 1) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
                     cudaSuccess ||
                 per_sm < 1)
                 return WGS_ERR_LAUNCH;
-            resident[dev.device].store(per_sm, std::memory_order_relaxed);
+            resident[dev.device].store((static_cast<int64_t>(threads) << 32) | per_sm,
+                                       std::memory_order_relaxed);
         }
         const int64_t blocks = ceil_div(rows, static_cast<int64_t>(rp) * U);
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
