@@ -350,8 +350,11 @@ def test_gelu_f16_full_size():
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
 @pytest.mark.parametrize("rows,width", [(1, 1), (3, 7), (5, 3), (17, 768), (1025, 1536),
-                                        (33, 1000), (2, 4100)])
+                                        (33, 1000), (2, 4100), (1, 768), (7, 1536),
+                                        (4097, 512), (3, 2048), (100, 256), (70000, 1024)])
 def test_gelu_widths_and_paths(rows, width, dtype):
+    """Grid-stride path, bulk-copy pipeline (rows of 64..256 16-byte chunks:
+    fewer rows than CTAs, one row, ragged last tiles) and the scalar path."""
     x, b = synth.gelu_input(rows, width, dtype, seed=rows + width)
     y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
     o, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
@@ -359,6 +362,18 @@ def test_gelu_widths_and_paths(rows, width, dtype):
         check_gelu_f32(np_(y), y64, f"gelu {rows}x{width}")
     else:
         check_fp16_near(np_(y), o, y64, f"gelu16 {rows}x{width}")
+    wgs.check_error(DEV)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_gelu_in_place_on_every_path(dtype):
+    for rows, width in ((2000, 1536), (999, 40), (64, 4104)):
+        x, b = synth.gelu_input(rows, width, dtype, seed=width)
+        xd = x.to(DEV)
+        want = wgs.bias_gelu_tanh(xd, b.to(DEV))
+        wgs.bias_gelu_tanh(xd, b.to(DEV), out=xd)
+        assert torch.equal(xd.view(torch.uint8), want.view(torch.uint8)), (rows, width)
+    wgs.check_error(DEV)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
