@@ -490,6 +490,31 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def test_bf16_residual_add_every_pattern():
+    """The residual sum r = bf16(a + b) bit for bit on every bf16 pattern as
+    a (subnormals, signed zeros, infinities, NaN) against shuffled b, and on
+    pairs of subnormals."""
+    rng = np.random.default_rng(7)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    n = -(-pats.size // 192) * 192
+    a = np.resize(pats, n)
+    b = rng.permutation(np.resize(pats, n))
+    sub = np.concatenate([np.arange(1, 128, dtype=np.uint16), np.arange(0x8001, 0x8080, dtype=np.uint16)])
+    a2 = np.resize(rng.permutation(sub), 192 * 8)
+    b2 = np.resize(rng.permutation(sub), 192 * 8)
+    for x, y in ((a, b), (a2, b2)):
+        xa = torch.from_numpy(x.astype(np.int16)).view(torch.bfloat16).view(-1, 192)
+        xb = torch.from_numpy(y.astype(np.int16)).view(torch.bfloat16).view(-1, 192)
+        r, _ = wgs.residual_add_ln_fwd(xa.to(DEV), xb.to(DEV), EPS)
+        o_r, _ = oracle.residual_add_ln(x.reshape(-1, 192), y.reshape(-1, 192), EPS, fmt="bf16")
+        g = _bits(r).ravel()
+        w = o_r.ravel()
+        nan = lambda v: ((v & 0x7F80) == 0x7F80) & ((v & 0x7F) != 0)  # noqa: E731
+        assert np.array_equal(nan(g), nan(w))
+        ok = ~nan(w)
+        assert np.array_equal(g[ok], w[ok]), np.flatnonzero(g[ok] != w[ok])[:5]
+
+
 @pytest.mark.parametrize("stage", [synth.TINY_PADDED, synth.STAGE_192, synth.STAGE_384],
                          ids=lambda s: s.name)
 def test_bf16_layernorm_family(stage):

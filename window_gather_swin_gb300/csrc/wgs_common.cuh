@@ -122,9 +122,10 @@ __device__ __forceinline__ void set_word(uint4 &v, int j, uint32_t w) {
 
 // 16-bit element formats of the row kernels: two elements per 32-bit word.
 // to_f2 widens exactly; from_f2 rounds to nearest even; add2 returns
-// round(a + b) for each pair, which for both formats equals rounding the
-// binary32 sum once more (binary32 carries at least 2p + 2 bits for a
-// p-bit format, so the double rounding is innocuous).
+// round(a + b) for each pair with one native add.  For both formats that
+// also equals rounding the binary32 sum once more (binary32 carries at
+// least 2p + 2 bits for a p-bit format, so the double rounding is
+// innocuous), which is how the residual sum is specified.
 struct Fp16 {
     __device__ static float2 to_f2(uint32_t w) { return half2_to_float2(w); }
     __device__ static uint32_t from_f2(float a, float b) { return float2_to_half2(a, b); }
@@ -151,9 +152,11 @@ struct Bf16 {
         memcpy(&r, &h, 4);
         return r;
     }
+    // one correctly rounded bf16x2 add (PTX add.rn.bf16x2, sm_90 and later)
     __device__ static uint32_t add2(uint32_t a, uint32_t b) {
-        const float2 x = to_f2(a), y = to_f2(b);
-        return from_f2(x.x + y.x, x.y + y.y);
+        uint32_t r;
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
     }
 };
 

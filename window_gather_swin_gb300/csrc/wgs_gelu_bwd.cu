@@ -217,21 +217,21 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     if (active) {
         const uint4 bv = __ldg(bias + cv);
         const int64_t G = groups;
-        for (int64_t r = r0 + g; r < r1; r += R * G) {
+        const int64_t step = G * row_chunks;  // chunks between a thread's rows
+        int64_t off = (r0 + g) * row_chunks + cv;
+        for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
             uint4 gyv[R], xv[R];
 #pragma unroll
             for (int q = 0; q < R; ++q) {
-                const int64_t rr = r + q * G;
-                if (rr < r1) {
-                    gyv[q] = ld_stream(gy + rr * row_chunks + cv);
-                    xv[q] = ld_stream(x + rr * row_chunks + cv);
+                if (r + q * G < r1) {
+                    gyv[q] = ld_stream(gy + off + q * step);
+                    xv[q] = ld_stream(x + off + q * step);
                 }
             }
 #pragma unroll
             for (int q = 0; q < R; ++q) {
-                const int64_t rr = r + q * G;
-                if (rr < r1)
-                    st_stream(gx + rr * row_chunks + cv, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
+                if (r + q * G < r1)
+                    st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
             }
         }
     }
