@@ -476,9 +476,11 @@ def run_ours(args, rank, world, local):
                 "frac": round(kernels[dom]["gbs"] / peak, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes": calls[dom].bytes}
 
-    kernels_next = None
+    kernels_next = sweep = None
     if not args.only:
         kernels_next = run_isolated(build_next_calls(), dev, l2, peak, args.isolated_launches)
+        if not args.no_sweep:
+            sweep = gelu_rows_sweep(dev, l2, peak, args.isolated_launches)
 
     # Diagnostic: the same step launched eagerly with an event between
     # launches, which attributes the step's time to its kernels (each also
@@ -529,6 +531,7 @@ def run_ours(args, rank, world, local):
         "kernels": kernels,
         "kernels_in_step": in_step,
         "kernels_next": kernels_next,
+        "gelu_rows_sweep": sweep,
         "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": K * len(calls),
@@ -574,6 +577,43 @@ def run_isolated(calls, dev, l2, peak, launches):
                     "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                     "buffer_sets": n_sets, "launches": n})
         del g, sets
+    return out
+
+
+def gelu_rows_sweep(dev, l2, peak, launches):
+    """bias_gelu_tanh fp32 at width 768 from 1k to 256k rows: device time
+    per call when launches are graph-replayed back to back, and when each
+    call is launched eagerly from Python, which shows where the host launch
+    path, not HBM, sets the pace."""
+    import window_gather_swin_gb300 as wgs
+    calls = []
+    for k in range(9):
+        rows = 1024 << k
+        x, b = synth.gelu_input(rows, 768, torch.float32, seed=4)
+        calls.append(Call("bias_gelu_tanh", f"fp32 [{rows},768]", 8 * rows * 768 + 4 * 768,
+                          {"x": x, "bias": b}, {"y": ((rows, 768), torch.float32)},
+                          lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]),
+                          None, rows))
+    graphed = run_isolated(calls, dev, l2, peak, launches)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for c, gr in zip(calls, graphed):
+        n_sets = gr["buffer_sets"]
+        sets = device_sets([c], dev, n_sets)
+        n = max(50, 2 * n_sets)
+        for s in range(3):
+            c.run(sets[s % n_sets][0][0], sets[s % n_sets][1][0])
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for s in range(n):
+            c.run(sets[s % n_sets][0][0], sets[s % n_sets][1][0])
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append({"rows": c.rows, "bytes": c.bytes, "ms_per_call": gr["ms_per_call"],
+                    "gbs": gr["gbs"], "frac_of_measured": gr["frac_of_measured"],
+                    "eager_ms_per_call": round(a.elapsed_time(e) / n, 5)})
+        del sets
     return out
 
 
@@ -722,6 +762,8 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the GELU rows sweep (1k-256k rows at width 768)")
     p.add_argument("--no-attribution", action="store_true",
                    help="skip the eager per-launch attribution of the step")
     p.add_argument("--isolated-launches", type=int, default=200)
