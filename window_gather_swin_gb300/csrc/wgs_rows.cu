@@ -1,14 +1,18 @@
 // Row kernels of the block glue: no-affine LayerNorm, fused residual add +
-// LayerNorm, shifted-window gather and fused norm-then-gather (sm_103a).
+// LayerNorm, shifted-window gather, fused norm-then-gather, and the two
+// block-boundary fusions (window reverse + residual add + LayerNorm;
+// residual add + LayerNorm + window gather), for fp16 and bfloat16 rows
+// (sm_103a).
 //
 // Page "BW1000 gfx936 Pangu-Weather inference profiling":
 //   s3  fixed-width (192 / 384) LayerNorm, FP16 in and out, FP32 statistics
 //   s4  residual add + norm that keeps the FP16 rounding point
 //   s5  INT32-indexed window gather (-1 = zero row) and the fused
 //       norm-gather that never writes the normalised tensor
+//   s1, s7  the restore path after attention (window reverse)
 //
-// Design (GB300): all four are HBM-bound row streams, so there are no tensor
-// cores here.  A row of W fp16 values is W/8 16-byte chunks; LPR lanes share
+// Design (GB300): all are HBM-bound row streams, so there are no tensor
+// cores here.  A row of W 16-bit values is W/8 16-byte chunks; LPR lanes share
 // a row (8 lanes at W = 192, 16 at W = 384), each holding CPL = 3 chunks in
 // registers, so one warp-wide load instruction moves whole 128-byte lines.
 // The row never leaves registers between load, FP32 butterfly reductions and
