@@ -417,7 +417,9 @@ def run_ours(args, rank, world, local):
     init_dist(world, "nccl")
     calls = build_calls()
     if args.only:
-        calls = [c for c in calls + build_next_calls() if args.only in c.label]
+        want = args.only
+        calls = [c for c in calls + build_next_calls()
+                 if (c.label == want[1:] if want.startswith("=") else want in c.label)]
         if not calls:
             raise SystemExit(f"--only {args.only!r} matches no call")
     props = torch.cuda.get_device_properties(dev)
@@ -550,32 +552,39 @@ def run_isolated(calls, dev, l2, peak, launches):
     least 3x L2 between two uses of a set) captured in one CUDA graph and
     replayed until about `launches` launches ran.  In this steady state a
     launch pays for exactly its own traffic, including the write-back of its
-    own previous outputs.  ms per call = region time / launches."""
+    own previous outputs.  ms per call = region time / launches; the median,
+    min and p90 are over the per-call times of the single replays."""
     stream = torch.cuda.current_stream(dev)
     out = []
     for c in calls:
         n_sets = max(2, -(-3 * l2 // c.bytes))
         per_graph = max(20, 2 * n_sets)
-        reps = max(1, -(-launches // per_graph))
+        reps = max(10, -(-launches // per_graph))
         sets = device_sets([c], dev, n_sets)
         g = capture(lambda: [c.run(sets[s % n_sets][0][0], sets[s % n_sets][1][0])
                              for s in range(per_graph)], dev)
         g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # an event between replays: the per-call time of every replay gives
+        # the spread (median, min, p90) besides the overall mean
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
         torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(reps):
+        ev[0].record(stream)
+        for r in range(reps):
             g.replay()
-        b.record(stream)
+            ev[r + 1].record(stream)
         torch.cuda.synchronize(dev)
         n = reps * per_graph
-        ms = a.elapsed_time(b) / n
+        per = sorted(ev[r].elapsed_time(ev[r + 1]) / per_graph for r in range(reps))
+        ms = ev[0].elapsed_time(ev[reps]) / n
         gbs = c.bytes / (ms / 1e3) / 1e9
         out.append({"kernel": c.name, "workload": c.workload, "bytes": c.bytes,
                     "ms_per_call": round(ms, 5), "gbs": round(gbs, 1),
                     "frac_of_measured": round(gbs / peak, 4),
                     "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
-                    "buffer_sets": n_sets, "launches": n})
+                    "ms_per_call_median": round(statistics.median(per), 5),
+                    "ms_per_call_min": round(per[0], 5),
+                    "ms_per_call_p90": round(per[min(reps - 1, int(0.9 * reps))], 5),
+                    "replays": reps, "buffer_sets": n_sets, "launches": n})
         del g, sets
     return out
 
@@ -768,7 +777,8 @@ def main(argv=None):
                    help="skip the eager per-launch attribution of the step")
     p.add_argument("--isolated-launches", type=int, default=200)
     p.add_argument("--only", default=None,
-                   help="time only the calls whose label contains this text (profiling aid)")
+                   help="time only the calls whose label contains this text, or equals it "
+                        "when it starts with '=' (profiling aid)")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be >= 3")
