@@ -5,16 +5,21 @@
  * Sources (page title, section):
  *   [P1] "BW1000 gfx936 Pangu-Weather inference profiling"
  *        (l189.com news 2144533)
+ *        s1  the profile: LayerNorm, index_select (two per block), GELU
  *        s3  fixed-width LayerNorm, affine folded into the next Linear
  *        s4  fused residual add + norm, keeping the FP16 rounding point
  *        s5  window gather with a precomputed INT32 index protocol, and the
  *            fused norm-then-gather
+ *        s6, s7  the ops kept in the final combination (bias-mask, restore
+ *            path) and the fusions rejected
  *   [P3] "PyTorch + HIP fused bias + GELU on Hygon DCU"
  *        (forum.sourcefind.cn)
- *        s3  math semantics: tanh-approximate GELU of input + bias
+ *        s3  math semantics: tanh-approximate GELU of input + bias (backward
+ *            left out there; added here)
  *        s6  interface checks: clear errors for bad inputs, empty input
  *            launches nothing, work goes on the caller's stream, launch
  *            status is checked
+ *        s10, s12  other dtypes as hardening (bfloat16 here)
  *
  * Conventions shared by every device entry point
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,

@@ -300,3 +300,36 @@ def test_bias_mask_argument_errors(lib):
     assert f(A, B, None, R, A + 64, 4, 6, 144, 1, -100.0, 1, None) == ALIAS      # shifted out
     assert f(A, B, None, R, B, 4, 6, 144, 1, -100.0, 1, None) == ALIAS           # out = bias
     assert f(A, B, None, C + 16, C, 4, 6, 144, 1, -100.0, 1, None) == ALIAS      # region in out
+
+
+# -------------------------------------------- randomised host builders ----
+
+def test_host_builders_equal_oracle_on_random_grids():
+    """Library index map, inverse map and region labels against the oracle
+    on random grids, windows (including cut last windows), shifts of any
+    sign and size, explicit padded extents, both orders and mask axes."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=300, deadline=None, derandomize=True)
+    @hyp.given(st.data())
+    def run(data):
+        grid = tuple(data.draw(st.integers(1, 9)) for _ in range(3))
+        win = tuple(data.draw(st.integers(1, 5)) for _ in range(3))
+        shift = tuple(data.draw(st.integers(-20, 20)) for _ in range(3))
+        padded = None
+        if data.draw(st.booleans()):
+            padded = tuple(g + data.draw(st.integers(0, 6)) for g in grid)
+        flags = data.draw(st.integers(0, 1))
+        axes = data.draw(st.integers(0, 7))
+        idx = wgs.build_window_index(grid, win, shift, padded, flags).numpy()
+        assert np.array_equal(idx, oracle.build_window_index(grid, win, shift, padded, flags))
+        lab = wgs.build_shift_regions(grid, win, shift, padded, flags, axes).numpy()
+        assert np.array_equal(lab, oracle.build_shift_regions(grid, win, shift, padded, flags, axes))
+        n_tokens = grid[0] * grid[1] * grid[2]
+        covered = np.bincount(idx[idx >= 0], minlength=n_tokens)
+        if (covered == 1).all():   # the map names every token once
+            inv = wgs.build_window_inverse(grid, win, shift, padded, flags).numpy()
+            assert np.array_equal(inv, oracle.invert_window_index(idx, n_tokens))
+
+    run()
