@@ -48,7 +48,9 @@ def test_rn16_matches_numpy_on_random_doubles():
     rng = np.random.default_rng(11)
     mag = np.exp2(rng.uniform(-30.0, 17.0, 400_000))
     v = mag * rng.choice([-1.0, 1.0], mag.size)
-    assert np.array_equal(oracle.rn16(v).view(np.uint16), v.astype(np.float16).view(np.uint16))
+    with np.errstate(over="ignore"):   # values past 65520 round to +-inf, as intended
+        ref = v.astype(np.float16)
+    assert np.array_equal(oracle.rn16(v).view(np.uint16), ref.view(np.uint16))
 
 
 def test_rn16_ties_go_to_even_and_near_ties_to_nearest():
