@@ -17,8 +17,10 @@
 // registers, so one warp-wide load instruction moves whole 128-byte lines.
 // The row never leaves registers between load, FP32 butterfly reductions and
 // store; the statistics use the shifted-data two-pass method (see
-// ln_normalize).  Each warp works on U row groups at once so that every lane has
+// ln_normalize).  Each warp works on U row groups at once, so every lane has
 // U * CPL independent 16-byte loads in flight before its first reduction.
+// U = 1 measured best: with 40 warps resident per SM there is enough memory
+// parallelism, and the smaller CTAs fill the last partial wave better.
 #include <atomic>
 
 #include "wgs_common.cuh"
@@ -27,7 +29,7 @@
 #define WGS_ROW_WARPS 4      // warps per CTA
 #endif
 #ifndef WGS_ROW_U
-#define WGS_ROW_U 2          // row groups per warp per iteration
+#define WGS_ROW_U 1          // row groups per warp per iteration
 #endif
 #ifndef WGS_ROW_CTAS_PER_SM
 #define WGS_ROW_CTAS_PER_SM 64  // grid cap, in CTAs per SM (grid-stride beyond it)
