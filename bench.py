@@ -69,6 +69,15 @@ class Call:
         return f"{self.name} {self.workload}"
 
 
+# The workload both arms report: the ten launches of one step.
+STEP_CONFIG = {
+    "workload": ("block-glue hot path, both stages: ln, residual_add_ln, window_gather, "
+                 "norm_gather at [131040,192]->138240 and [32760,384]->34560; bias_gelu fp32 "
+                 "[131040,768], fp16 [32760,1536]"),
+    "window": list(synth.WINDOW), "shift": list(synth.SHIFT),
+}
+
+
 def build_calls():
     import window_gather_swin_gb300 as wgs
     calls = []
@@ -515,11 +524,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "storage_dtype": "fp16 rows (LN, gathers, fp16 GELU), fp32 (fp32 GELU)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": {"workload": ("block-glue hot path, both stages: ln, residual_add_ln, "
-                                "window_gather, norm_gather at [131040,192]->138240 and "
-                                "[32760,384]->34560; bias_gelu fp32 [131040,768], fp16 [32760,1536]"
-                                if not args.only else f"subset: {args.only}"),
-                   "window": list(synth.WINDOW), "shift": list(synth.SHIFT),
+        "config": {**(STEP_CONFIG if not args.only else {"workload": f"subset: {args.only}"}),
                    "launches_per_step": len(calls),
                    "l2": (f"inputs larger than L2: steps run back to back and one step touches "
                           f"{step_bytes * n_sets / 1e6:.0f} MB over {n_sets} buffer set(s) "
@@ -750,7 +755,9 @@ def run_reference(args, rank, world):
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": {"workload": "block-glue hot path, both stages (oracle on a row sample)",
+        "config": {**STEP_CONFIG, "launches_per_step": len(calls),
+                   "timing": ("each step runs the oracle on a row sample of every call of the step "
+                              "(see cpu_baseline.sample); time.perf_counter around each call"),
                    "parallelism": "rank 0 only"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
