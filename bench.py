@@ -734,7 +734,7 @@ def run_reference(args, rank, world):
     probe = 1.0 / 1024
     probe_s = sum(c.oracle_run(probe)[0] for c in calls)
     full_step_s = probe_s / probe
-    budget_s = 120.0
+    budget_s = args.ref_budget_s
     frac = budget_s / (full_step_s * (args.steps + args.warmup))
     frac = max(1.0 / 16384, min(1.0 / 16, frac))
     for _ in range(args.warmup):
@@ -778,6 +778,8 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--ref-budget-s", type=float, default=120.0,
+                   help="--impl reference: seconds of oracle work to aim for over the whole run")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the GELU rows sweep (1k-256k rows at width 768)")
     p.add_argument("--no-attribution", action="store_true",

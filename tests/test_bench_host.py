@@ -48,3 +48,24 @@ def test_two_gloo_ranks_aggregate_like_the_bench():
 def test_single_rank_reductions_are_identity():
     assert bench.reduce_max(3.0, 1, None) == 3.0
     assert bench.reduce_sum(4.0, 1, None) == 4.0
+
+
+def test_reference_arm_under_two_ranks_prints_one_line():
+    """torchrun with two CPU ranks: rank 0 times the oracle and prints one
+    JSON line with the arm's fields, rank 1 exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "1", "--ref-budget-s", "2"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["workload"] == bench.STEP_CONFIG["workload"]
