@@ -39,6 +39,10 @@
  *   - Calls are thread-safe; the shared state is the per-device index
  *     error word read by wgs_check_error() (and the scratch array of
  *     bias_gelu_tanh_bwd_noalloc).
+ *   - The first call of an entry point on a device caches what it needs
+ *     from the runtime (SM count, resident CTAs per SM, symbol addresses);
+ *     make that call outside stream capture.  Later calls, captured or
+ *     not, make no such query.
  */
 #ifndef WGS_H
 #define WGS_H
