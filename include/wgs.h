@@ -40,9 +40,10 @@
  *     error word read by wgs_check_error() (and the scratch array of
  *     bias_gelu_tanh_bwd_noalloc).
  *   - The first call of an entry point on a device caches what it needs
- *     from the runtime (SM count, resident CTAs per SM, symbol addresses);
- *     make that call outside stream capture.  Later calls, captured or
- *     not, make no such query.
+ *     from the runtime (SM count, resident CTAs per SM, symbol addresses),
+ *     and so does window_bias_mask_add's first call with a new n; make those
+ *     calls outside stream capture.  Other calls, captured or not, make no
+ *     such query.
  */
 #ifndef WGS_H
 #define WGS_H
