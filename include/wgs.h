@@ -39,7 +39,7 @@
  *   - Calls are thread-safe; the shared state is the per-device index
  *     error word read by wgs_check_error() (and the scratch array of
  *     bias_gelu_tanh_bwd_noalloc).
- *   - The first call of an entry point on a device caches what it needs
+ *   - The first call of an entry point on a device (per dtype) caches what it needs
  *     from the runtime (SM count, resident CTAs per SM, symbol addresses),
  *     and so does window_bias_mask_add's first call with a new n; make those
  *     calls outside stream capture.  Other calls, captured or not, make no
