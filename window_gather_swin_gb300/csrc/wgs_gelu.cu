@@ -35,6 +35,9 @@
 #ifndef WGS_GELU_U
 #define WGS_GELU_U 4
 #endif
+#ifndef WGS_GELU_U16
+#define WGS_GELU_U16 2  // chunks per thread per pass for 16-bit data, with prefetch
+#endif
 #ifndef WGS_GELU_CTAS_PER_SM
 #define WGS_GELU_CTAS_PER_SM 0  // grid cap in CTAs per SM; 0: as many as can be resident
 #endif
@@ -145,7 +148,9 @@ __device__ __forceinline__ uint4 gelu_chunk(const uint4 &xv, const uint4 &bv) {
 // Flat grid-stride over 16-byte chunks.  Chunk i belongs to column chunk
 // i mod row_vecs; each thread tracks that column incrementally (all steps
 // are below row_vecs, so one conditional subtraction keeps it in range).
-template <typename E, int U, int THREADS>
+// With PF the x chunks of the next pass are loaded before this pass's
+// arithmetic, so each thread keeps loads in flight while it computes.
+template <typename E, int U, int THREADS, bool PF>
 __global__ void WGS_GELU_BOUNDS(THREADS)
 bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec, int32_t row_vecs) {
     pdl_prologue();
@@ -155,6 +160,39 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
     const int32_t per_iter = static_cast<int32_t>(stride % row_vecs);
     int64_t i0 = static_cast<int64_t>(blockIdx.x) * kTile + threadIdx.x;
     int32_t col0 = static_cast<int32_t>(i0 % row_vecs);
+    if constexpr (PF) {
+        // x chunks of the next pass load while this pass computes
+        uint4 nx[U];
+        auto fetch = [&](int64_t base, uint4 *dst) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + static_cast<int64_t>(u) * THREADS;
+                if (i < n_vec) dst[u] = ld_stream(x + i);
+            }
+        };
+        fetch(i0, nx);
+        for (; i0 < n_vec; i0 += stride) {
+            uint4 xv[U], bv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) xv[u] = nx[u];
+            fetch(i0 + stride, nx);
+            int32_t col = col0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                bv[u] = __ldg(bias + col);
+                col += in_tile;
+                if (col >= row_vecs) col -= row_vecs;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
+                if (i < n_vec) st_stream(y + i, gelu_chunk<E>(xv[u], bv[u]));
+            }
+            col0 += per_iter;
+            if (col0 >= row_vecs) col0 -= row_vecs;
+        }
+        return;
+    }
     for (; i0 < n_vec; i0 += stride) {
         uint4 xv[U], bv[U];
         int32_t col = col0;
@@ -207,12 +245,16 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
     const int64_t n = rows * width;
     const bool vec = width % kVec == 0 && aligned16(x) && aligned16(bias) && aligned16(y);
     if (vec) {
-        constexpr int T = WGS_GELU_THREADS, U = WGS_GELU_U;
+        // 16-bit data: fewer chunks per pass, the next pass's loads issued
+        // before this pass computes (eight elements a chunk make the compute
+        // long enough to hide behind them); fp32: more chunks, no prefetch
+        constexpr bool PF = !std::is_same<E, F32>::value;
+        constexpr int T = WGS_GELU_THREADS, U = PF ? WGS_GELU_U16 : WGS_GELU_U;
         const int64_t n_vec = n / kVec;
         const int64_t need = ceil_div(n_vec, static_cast<int64_t>(T) * U);
         // One resident wave of grid-stride CTAs: a partial second wave
         // would leave SMs idle at the end of this bandwidth-bound stream.
-        auto kernel = bias_gelu_vec_kernel<E, U, T>;
+        auto kernel = bias_gelu_vec_kernel<E, U, T, PF>;
         static std::atomic<int> resident[64];  // per device, for this instantiation
         int per_sm = WGS_GELU_CTAS_PER_SM > 0 ? WGS_GELU_CTAS_PER_SM
                                               : resident[device].load(std::memory_order_relaxed);
