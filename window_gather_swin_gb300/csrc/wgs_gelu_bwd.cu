@@ -39,7 +39,10 @@
 #define WGS_BWD_ROWS 4  // rows in flight per thread, fp32
 #endif
 #ifndef WGS_BWD_ROWS16
-#define WGS_BWD_ROWS16 3  // rows in flight per thread, 16-bit formats
+#define WGS_BWD_ROWS16 2  // rows per step per thread, 16-bit formats (two steps in flight)
+#endif
+#ifndef WGS_BWD_PF16
+#define WGS_BWD_PF16 1  // 16-bit: load the next rows while computing these
 #endif
 #ifndef WGS_BWD_GROUPS
 #define WGS_BWD_GROUPS 4  // most row groups per CTA
@@ -214,7 +217,7 @@ __device__ __forceinline__ uint4 grad_chunk(const uint4 &gyv, const uint4 &xv, c
 // column chunk blockIdx.y * CVB + j and walks rows r0 + g, r0 + g + G, ...
 // of its slab, R rows in flight at a time, accumulating them in
 // increasing row order.
-template <typename E, int R>
+template <typename E, int R, bool PF>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
                 int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
@@ -235,19 +238,42 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
         const int64_t G = groups;
         const int64_t step = G * row_chunks;  // chunks between a thread's rows
         int64_t off = (r0 + g) * row_chunks + cv;
-        for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
-            uint4 gyv[R], xv[R];
+        auto fetch = [&](int64_t r, int64_t o, uint4 *gyv, uint4 *xv) {
 #pragma unroll
             for (int q = 0; q < R; ++q) {
                 if (r + q * G < r1) {
-                    gyv[q] = ld_stream(gy + off + q * step);
-                    xv[q] = ld_stream(x + off + q * step);
+                    gyv[q] = ld_stream(gy + o + q * step);
+                    xv[q] = ld_stream(x + o + q * step);
                 }
             }
+        };
+        if constexpr (PF) {
+            // the next R rows load while these R compute
+            uint4 ngy[R], nx[R];
+            fetch(r0 + g, off, ngy, nx);
+            for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
+                uint4 gyv[R], xv[R];
 #pragma unroll
-            for (int q = 0; q < R; ++q) {
-                if (r + q * G < r1)
-                    st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
+                for (int q = 0; q < R; ++q) {
+                    gyv[q] = ngy[q];
+                    xv[q] = nx[q];
+                }
+                fetch(r + R * G, off + R * step, ngy, nx);
+#pragma unroll
+                for (int q = 0; q < R; ++q) {
+                    if (r + q * G < r1)
+                        st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
+                }
+            }
+        } else {
+            for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
+                uint4 gyv[R], xv[R];
+                fetch(r, off, gyv, xv);
+#pragma unroll
+                for (int q = 0; q < R; ++q) {
+                    if (r + q * G < r1)
+                        st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
+                }
             }
         }
     }
@@ -375,7 +401,7 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
     wgs_status st;
     if (chunks) {
         const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
-        st = launch(gelu_bwd_chunks<E, k16 ? WGS_BWD_ROWS16 : WGS_BWD_ROWS>, grid, block, smem, stream,
+        st = launch(gelu_bwd_chunks<E, k16 ? WGS_BWD_ROWS16 : WGS_BWD_ROWS, k16 && WGS_BWD_PF16>, grid, block, smem, stream,
                     static_cast<const uint4 *>(gy), static_cast<const uint4 *>(x),
                     static_cast<const uint4 *>(bias), static_cast<uint4 *>(gx), partial, rows,
                     units, width, cvb, groups, slabs);
