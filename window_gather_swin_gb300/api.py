@@ -92,7 +92,8 @@ def ln_fwd(x: torch.Tensor, eps: float = 1e-5, out: Optional[torch.Tensor] = Non
 def residual_add_ln_fwd(residual: torch.Tensor, branch: torch.Tensor, eps: float = 1e-5,
                         residual_out: Optional[torch.Tensor] = None,
                         out: Optional[torch.Tensor] = None):
-    """Returns (residual_out, y): residual_out = fp16(residual + branch),
+    """Returns (residual_out, y): residual_out = round(residual + branch) in
+    the tensors' 16-bit format (fp16 or bfloat16),
     y = LN(residual_out)."""
     _row16(residual, "residual")
     _cuda(branch, "branch", residual.dtype)
@@ -151,7 +152,7 @@ def window_reverse_add_ln_fwd(residual: torch.Tensor, windows: torch.Tensor,
                               inv_idx: torch.Tensor, eps: float = 1e-5,
                               residual_out: Optional[torch.Tensor] = None,
                               out: Optional[torch.Tensor] = None):
-    """Returns (residual_out, y): residual_out[t] = fp16(residual[t] +
+    """Returns (residual_out, y): residual_out[t] = round(residual[t] +
     windows[inv_idx[t]]), y = LN(residual_out)."""
     _row16(residual, "residual")
     _cuda(windows, "windows", residual.dtype)
@@ -174,7 +175,7 @@ def window_reverse_add_ln_fwd(residual: torch.Tensor, windows: torch.Tensor,
 def residual_add_norm_gather(residual: torch.Tensor, branch: torch.Tensor, idx: torch.Tensor,
                              eps: float = 1e-5, residual_out: Optional[torch.Tensor] = None,
                              out: Optional[torch.Tensor] = None):
-    """Returns (residual_out, dst): residual_out = fp16(residual + branch),
+    """Returns (residual_out, dst): residual_out = round(residual + branch),
     dst[d] = LN(residual_out)[idx[d]] (zero row for -1)."""
     _row16(residual, "residual")
     _cuda(branch, "branch", residual.dtype)
