@@ -121,12 +121,27 @@ __device__ __forceinline__ void set_word(uint4 &v, int j, uint32_t w) {
 }
 
 // 16-bit element formats of the row kernels: two elements per 32-bit word.
-// to_f2 widens exactly; from_f2 rounds to nearest even; add2 returns
+// to_f2 widens exactly; widen_add2 widens and adds an FP32 pair (one
+// rounding); from_f2 rounds to nearest even; add2 returns
 // round(a + b) for each pair with one native add.  For both formats that
 // also equals rounding the binary32 sum once more (binary32 carries at
 // least 2p + 2 bits for a p-bit format, so the double rounding is
 // innocuous), which is how the residual sum is specified.
+// (lo + c.x, hi + c.y) for the two 16-bit values of word w, each widened
+// exactly and added in FP32 with one rounding: PTX add.rn.f32.f16 / .bf16
+// (widen and add in one instruction).
+#define WGS_WIDEN_ADD2(FMT)                                                              \
+    __device__ static float2 widen_add2(uint32_t w, float2 c) {                        \
+        float2 r;                                                                       \
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"                       \
+            "add.rn.f32." FMT " %0, lo, %3;\n\tadd.rn.f32." FMT " %1, hi, %4;\n\t}"         \
+            : "=f"(r.x), "=f"(r.y)                                                      \
+            : "r"(w), "f"(c.x), "f"(c.y));                                              \
+        return r;                                                                       \
+    }
+
 struct Fp16 {
+    WGS_WIDEN_ADD2("f16")
     __device__ static float2 to_f2(uint32_t w) { return half2_to_float2(w); }
     __device__ static uint32_t from_f2(float a, float b) { return float2_to_half2(a, b); }
     __device__ static uint32_t add2(uint32_t a, uint32_t b) {
@@ -141,6 +156,7 @@ struct Fp16 {
 };
 
 struct Bf16 {
+    WGS_WIDEN_ADD2("bf16")
     __device__ static float2 to_f2(uint32_t w) {
         __nv_bfloat162 h;
         memcpy(&h, &w, 4);

@@ -155,22 +155,6 @@ __device__ __forceinline__ void put_pair(uint4 &out, int w, float2 v) {
     }
 }
 
-// acc + the two 16-bit values of a word, each widened exactly and added in
-// FP32 (PTX add.rn.f32.f16 / .bf16: one instruction, no separate convert).
-template <typename E>
-__device__ __forceinline__ float2 add_word(float2 acc, uint32_t w) {
-    float2 r;
-    if constexpr (std::is_same<E, Bf16>::value)
-        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-            "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
-            : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(acc.x), "f"(acc.y));
-    else
-        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-            "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
-            : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(acc.x), "f"(acc.y));
-    return r;
-}
-
 // The chunk with gelu_grad chosen per element (far-left elements in FP64);
 // only chunks holding some t < -4 come here.
 template <typename E, bool k16>
@@ -205,7 +189,7 @@ __device__ __forceinline__ uint4 grad_chunk(const uint4 &gyv, const uint4 &xv, c
 #pragma unroll
     for (int w = 0; w < kPairs; ++w) {
         if constexpr (k16)
-            acc[w] = add_word<E>(acc[w], word(out, w));
+            acc[w] = E::widen_add2(word(out, w), acc[w]);
         else
             acc[w] = __fadd2_rn(acc[w], make_float2(__uint_as_float(word(out, 2 * w)),
                                                     __uint_as_float(word(out, 2 * w + 1))));
