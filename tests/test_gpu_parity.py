@@ -376,6 +376,19 @@ def test_gelu_in_place_on_every_path(dtype):
     wgs.check_error(DEV)
 
 
+def test_gelu_largest_sweep_size_on_sampled_rows():
+    """fp32 [262144, 768] (the top of the rows sweep, 1.6 GB moved): 4096
+    sampled rows against the oracle, one by one."""
+    rows, width = 262144, 768
+    x, b = synth.gelu_input(rows, width, torch.float32, seed=4)
+    y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
+    pick = np.sort(np.random.default_rng(0).choice(rows, 4096, replace=False))
+    xs = x.numpy()[pick]
+    _, y64 = oracle.bias_gelu_tanh(xs, b.numpy())
+    check_gelu_f32(np_(y)[pick], y64, "gelu f32 262144 rows, sampled")
+    wgs.check_error(DEV)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
 def test_gelu_misaligned_views_take_the_scalar_path(dtype):
     x, b = synth.gelu_input(65, 769, dtype, seed=3)
