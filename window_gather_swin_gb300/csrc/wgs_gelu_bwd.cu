@@ -36,13 +36,7 @@
 #include "wgs_common.cuh"
 
 #ifndef WGS_BWD_ROWS
-#define WGS_BWD_ROWS 4  // rows in flight per thread, fp32
-#endif
-#ifndef WGS_BWD_ROWS16
-#define WGS_BWD_ROWS16 2  // rows per step per thread, 16-bit formats (two steps in flight)
-#endif
-#ifndef WGS_BWD_PF16
-#define WGS_BWD_PF16 1  // 16-bit: load the next rows while computing these
+#define WGS_BWD_ROWS 2  // rows per step per thread (two steps in flight)
 #endif
 #ifndef WGS_BWD_GROUPS
 #define WGS_BWD_GROUPS 4  // most row groups per CTA
@@ -199,9 +193,10 @@ __device__ __forceinline__ uint4 grad_chunk(const uint4 &gyv, const uint4 &xv, c
 
 // Pass 1, 16-byte chunks.  Block = CVB * G threads: thread (g, j) owns
 // column chunk blockIdx.y * CVB + j and walks rows r0 + g, r0 + g + G, ...
-// of its slab, R rows in flight at a time, accumulating them in
-// increasing row order.
-template <typename E, int R, bool PF>
+// of its slab, R rows a step, accumulating them in increasing row order.
+// The next step's loads are issued before this step's arithmetic, so each
+// thread keeps loads in flight while it computes.
+template <typename E, int R>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
                 int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
@@ -231,33 +226,21 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
                 }
             }
         };
-        if constexpr (PF) {
-            // the next R rows load while these R compute
-            uint4 ngy[R], nx[R];
-            fetch(r0 + g, off, ngy, nx);
-            for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
-                uint4 gyv[R], xv[R];
+        // the next R rows load while these R compute
+        uint4 ngy[R], nx[R];
+        fetch(r0 + g, off, ngy, nx);
+        for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
+            uint4 gyv[R], xv[R];
 #pragma unroll
-                for (int q = 0; q < R; ++q) {
-                    gyv[q] = ngy[q];
-                    xv[q] = nx[q];
-                }
-                fetch(r + R * G, off + R * step, ngy, nx);
-#pragma unroll
-                for (int q = 0; q < R; ++q) {
-                    if (r + q * G < r1)
-                        st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
-                }
+            for (int q = 0; q < R; ++q) {
+                gyv[q] = ngy[q];
+                xv[q] = nx[q];
             }
-        } else {
-            for (int64_t r = r0 + g; r < r1; r += R * G, off += R * step) {
-                uint4 gyv[R], xv[R];
-                fetch(r, off, gyv, xv);
+            fetch(r + R * G, off + R * step, ngy, nx);
 #pragma unroll
-                for (int q = 0; q < R; ++q) {
-                    if (r + q * G < r1)
-                        st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
-                }
+            for (int q = 0; q < R; ++q) {
+                if (r + q * G < r1)
+                    st_stream(gx + off + q * step, grad_chunk<E, k16>(gyv[q], xv[q], bv, acc));
             }
         }
     }
@@ -385,7 +368,7 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
     wgs_status st;
     if (chunks) {
         const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
-        st = launch(gelu_bwd_chunks<E, k16 ? WGS_BWD_ROWS16 : WGS_BWD_ROWS, k16 && WGS_BWD_PF16>, grid, block, smem, stream,
+        st = launch(gelu_bwd_chunks<E, WGS_BWD_ROWS>, grid, block, smem, stream,
                     static_cast<const uint4 *>(gy), static_cast<const uint4 *>(x),
                     static_cast<const uint4 *>(bias), static_cast<uint4 *>(gx), partial, rows,
                     units, width, cvb, groups, slabs);
