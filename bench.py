@@ -11,6 +11,10 @@ Window (2,6,12), shift (1,3,6).  Inputs are seeded synthetic tensors.
 
 Metric: effective HBM GB/s (algorithmic bytes: each input read once, each
 output written once, plus the index array) and ms per call per kernel.
+Beyond the step the line carries the other rows of the path (block-boundary
+fusions, bfloat16 forms, the GELU backward, the attention bias-mask add),
+a GELU rows sweep (1k-256k rows), the end-to-end figure from pinned host
+memory, and the oracle's single-thread CPU rate.
 A step's ten launches are captured once, through the public API, in a CUDA
 graph; the graph is replayed K times back to back and CUDA events on the
 launching stream bracket the K replays.  One step touches 1.77 GB (13x the
@@ -771,12 +775,15 @@ def run_reference(args, rank, world):
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
-    p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--gpus", type=int, default=1, help="ranks (one GPU each) of the run")
+    p.add_argument("--steps", type=int, default=2000, help="timed steps")
+    p.add_argument("--warmup", type=int, default=5, help="untimed steps before the timed ones")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                   help="ours: the CUDA library; reference: the CPU oracle on a row sample")
+    p.add_argument("--e2e-steps", type=int, default=20,
+                   help="steps of the end-to-end leg from pinned host memory (at most --steps)")
+    p.add_argument("--no-cpu-baseline", action="store_true",
+                   help="skip timing the oracle on the host cores")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--ref-budget-s", type=float, default=120.0,
                    help="--impl reference: seconds of oracle work to aim for over the whole run")
@@ -784,7 +791,8 @@ def main(argv=None):
                    help="skip the GELU rows sweep (1k-256k rows at width 768)")
     p.add_argument("--no-attribution", action="store_true",
                    help="skip the eager per-launch attribution of the step")
-    p.add_argument("--isolated-launches", type=int, default=200)
+    p.add_argument("--isolated-launches", type=int, default=200,
+                   help="launches per kernel when each kernel is timed alone")
     p.add_argument("--only", default=None,
                    help="time only the calls whose label contains this text, or equals it "
                         "when it starts with '=' (profiling aid)")
