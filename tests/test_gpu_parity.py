@@ -477,6 +477,49 @@ def test_runs_on_the_callers_stream():
     assert torch.equal(y.view(torch.int16), want.view(torch.int16))
 
 
+def test_concurrent_streams_and_host_threads_give_the_sequential_bits():
+    """Different entry points running at once on four streams, launched from
+    four host threads, each repeated: every output equals its sequential
+    run bit for bit (the library keeps no per-call state)."""
+    import threading
+    dev = torch.device(DEV)
+    st = synth.STAGE_192
+    a, b = synth.residual_branch(st.tokens, st.width, seed=2)
+    a, b = a.to(dev), b.to(dev)
+    idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded).to(dev)
+    xg, bg = synth.gelu_input(32760, 1536, torch.float16, seed=4)
+    gy, _ = synth.gelu_input(32760, 1536, torch.float16, seed=5)
+    xg, bg, gy = xg.to(dev), bg.to(dev), gy.to(dev)
+    sc, sb = synth.attention_logits(256, 12, 144, 1, seed=6)
+    sc, sb = sc.to(dev), sb.to(dev)
+    reg = wgs.build_shift_regions(synth.ATTN_384.grid, synth.WINDOW, synth.SHIFT,
+                                  synth.ATTN_384.padded).to(dev)
+    jobs = [lambda: wgs.residual_add_norm_gather(a, b, idx, EPS),
+            lambda: wgs.bias_gelu_tanh(xg, bg),
+            lambda: wgs.bias_gelu_tanh_bwd(gy, xg, bg),
+            lambda: wgs.window_bias_mask_add(sc, sb, None, reg)]
+    want = [j() for j in jobs]
+    torch.cuda.synchronize(dev)
+    got = [None] * len(jobs)
+
+    def run(k):
+        with torch.cuda.device(dev), torch.cuda.stream(torch.cuda.Stream(device=dev)):
+            for _ in range(3):
+                got[k] = jobs[k]()
+            torch.cuda.current_stream(dev).synchronize()
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    flat = lambda r: list(r) if isinstance(r, tuple) else [r]  # noqa: E731
+    for k in range(len(jobs)):
+        for g, w in zip(flat(got[k]), flat(want[k])):
+            assert torch.equal(g.view(torch.uint8), w.view(torch.uint8)), k
+    wgs.check_error(DEV)
+
+
 # ---------------------------------------------------- contract checks ----
 
 def test_python_contract_errors():
