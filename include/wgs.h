@@ -253,10 +253,11 @@ wgs_status bias_gelu_tanh(const void *x, const void *bias, void *y, int64_t rows
  *          other overlaps return WGS_ERR_ALIAS.
  *   bias, grad_bias    [width] of `dtype`, disjoint from everything else.
  *   workspace  device memory of at least
- *          wgs_bias_gelu_bwd_workspace_bytes(rows, width) bytes, 16-byte
- *          aligned, owned by the caller, disjoint from the tensors; its
- *          contents on entry do not matter.
- *   rows == 0 writes grad_bias = 0 (one small launch); width == 0 returns
+ *          wgs_bias_gelu_bwd_workspace_bytes(rows, width) bytes (one slab of
+ *          width floats when rows == 0), 16-byte aligned, owned by the
+ *          caller, disjoint from the tensors; its contents on entry do not
+ *          matter.
+ *   rows == 0 writes grad_bias = 0 (two small launches); width == 0 returns
  *   WGS_OK and launches nothing.  The 16-byte vector path needs width a
  *   multiple of 4 (f32) or 8 (16-bit types) and aligned tensors; otherwise
  *   a scalar path runs (same results). */

@@ -227,7 +227,8 @@ def test_gelu_backward_argument_errors(lib):
     need = lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 768)
     assert need == 8 * 768 * 4                       # 1000 rows -> 8 slabs of >= 128 rows
     assert lib.wgs_bias_gelu_bwd_workspace_bytes(131040, 768) == 512 * 768 * 4
-    assert lib.wgs_bias_gelu_bwd_workspace_bytes(0, 768) == 0
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(0, 768) == 768 * 4   # one slab: grad_bias = 0
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 0) == 0
     W = 0x50000000
     assert f(A, B, C, D, A + 2 ** 24, W, need, 1000, 768, 5, None) == DTYPE
     assert f(A, B, C, D, A + 2 ** 24, W, need, -1, 768, 0, None) == SHAPE

@@ -218,7 +218,7 @@ def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
 
 def gelu_bwd_workspace_bytes(rows: int, width: int) -> int:
     """Bytes of workspace bias_gelu_tanh_bwd needs for a [rows, width] tensor."""
-    return int(_capi.load().wgs_bias_gelu_bwd_workspace_bytes(max(int(rows), 1), int(width)))
+    return int(_capi.load().wgs_bias_gelu_bwd_workspace_bytes(int(rows), int(width)))
 
 
 def bias_gelu_tanh_bwd(grad_y: torch.Tensor, x: torch.Tensor, bias: torch.Tensor,
@@ -241,7 +241,7 @@ def bias_gelu_tanh_bwd(grad_y: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
     gx = _out(grad_x, x.shape, x.dtype, x.device, "grad_x")
     gb = _out(grad_bias, bias.shape, x.dtype, x.device, "grad_bias")
     lib = _capi.load()
-    need = int(lib.wgs_bias_gelu_bwd_workspace_bytes(max(rows, 1), width))
+    need = int(lib.wgs_bias_gelu_bwd_workspace_bytes(rows, width))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _cuda(workspace, "workspace", torch.uint8)

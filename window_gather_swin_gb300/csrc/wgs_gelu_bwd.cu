@@ -385,9 +385,11 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
 
 }  // namespace
 
+// Zero rows still take one slab: pass 2 then writes grad_bias = 0.
 size_t bwd_workspace_bytes(int64_t rows, int32_t width) {
-    if (rows <= 0 || width <= 0) return 0;
-    return static_cast<size_t>(slabs_for(rows)) * static_cast<size_t>(width) * sizeof(float);
+    if (width <= 0) return 0;
+    return static_cast<size_t>(slabs_for(rows > 0 ? rows : 1)) * static_cast<size_t>(width) *
+           sizeof(float);
 }
 
 wgs_status bias_gelu_bwd_checked(const void *grad_y, const void *x, const void *bias,
@@ -444,7 +446,7 @@ extern "C" wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, cons
                                          wgs_dtype dtype, cudaStream_t stream) {
     wgs_status st = bias_gelu_bwd_args(grad_y, x, bias, grad_x, grad_bias, rows, width, dtype);
     if (st != WGS_OK || width == 0) return st;
-    const size_t need = bwd_workspace_bytes(rows > 0 ? rows : 1, width);
+    const size_t need = bwd_workspace_bytes(rows, width);
     if (!workspace) return WGS_ERR_NULL;
     if (workspace_bytes < need) return WGS_ERR_SHAPE;
     if (!aligned16(workspace)) return WGS_ERR_ALIGN;
@@ -506,7 +508,7 @@ extern "C" wgs_status bias_gelu_tanh_bwd_noalloc(const void *grad_y, const void 
                                                  cudaStream_t stream) {
     const wgs_status st = bias_gelu_bwd_args(grad_y, x, bias, grad_x, grad_bias, rows, width, dtype);
     if (st != WGS_OK || width == 0) return st;
-    if (bwd_workspace_bytes(rows > 0 ? rows : 1, width) > kNoAllocScratchFloats * sizeof(float))
+    if (bwd_workspace_bytes(rows, width) > kNoAllocScratchFloats * sizeof(float))
         return WGS_ERR_TOO_LARGE;
     DeviceInfo dev;
     const wgs_status ds = current_device(&dev);
