@@ -55,7 +55,11 @@
 extern "C" {
 #endif
 
-#define WGS_ABI_VERSION 1
+/* 1: the LayerNorm family, gathers and bias + GELU in fp16 / fp32.
+ * 2: adds the bfloat16 forms, the GELU backward (with and without a
+ *    workspace), the attention bias-mask add and the region-label builder;
+ *    the backward's workspace query covers zero rows. */
+#define WGS_ABI_VERSION 2
 
 typedef enum {
     WGS_OK = 0,

@@ -50,7 +50,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.wgs_abi_version() == 1
+    assert lib.wgs_abi_version() == 2
     for s in range(11):
         assert lib.wgs_status_string(s)
     assert b"unknown" in lib.wgs_status_string(99)

@@ -17,6 +17,7 @@ STATUS_NAMES = {
     8: "WGS_ERR_INDEX", 9: "WGS_ERR_ALIAS", 10: "WGS_ERR_CUDA", 11: "WGS_ERR_TOO_LARGE",
 }
 WGS_F32, WGS_F16, WGS_BF16 = 0, 1, 2
+ABI_VERSION = 2  # WGS_ABI_VERSION of include/wgs.h that these signatures describe
 
 _P = ctypes.c_void_p
 _i64, _i32, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
@@ -83,6 +84,9 @@ def load(path: str | None = None):
             fn = getattr(lib, name)  # AttributeError: the library lacks an entry point
             fn.restype = res
             fn.argtypes = args
+        if lib.wgs_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{path} has ABI version {lib.wgs_abi_version()}, this binding "
+                               f"expects {ABI_VERSION}: rebuild it")
         _lib = lib
         return lib
 
