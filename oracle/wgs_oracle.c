@@ -13,8 +13,13 @@
  *        2144533): s3 fixed-width LayerNorm, s4 residual add + norm and its
  *        FP16 rounding point, s5 window gather with the INT32 index protocol
  *        and the fused norm-gather.
+ *        s1, s7 the restore path after attention; s6, s7 the "bias-mask" op
+ *        kept in the final combination (its arithmetic is a reading, see
+ *        orc_window_bias_mask_add_fmt).
  *   [P3] "PyTorch + HIP fused bias + GELU on Hygon DCU" (forum.sourcefind.cn):
- *        s3 math semantics (tanh-approximate GELU of input + bias).
+ *        s3 math semantics (tanh-approximate GELU of input + bias); the
+ *        backward it leaves out is the derivative of that formula.
+ *        s10, s12 other formats as hardening (bfloat16 here).
  *
  * fp16 values travel as their IEEE binary16 bit patterns (uint16_t).
  */
