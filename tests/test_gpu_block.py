@@ -102,10 +102,10 @@ def _block_reference(x, w, grid, padded, heads):
     return r + m
 
 
-def _block_library(x, w, grid, padded, heads):
-    """fp16, glue on the library."""
+def _block_library(x, w, grid, padded, heads, dtype):
+    """x's 16-bit format throughout, glue on the library."""
     c = x.shape[1]
-    w = {k: v.half() for k, v in w.items()}
+    w = {k: v.to(dtype) for k, v in w.items()}
     idx = wgs.build_window_index(grid, synth.WINDOW, synth.SHIFT, padded, device=DEV)
     inv = wgs.build_window_inverse(grid, synth.WINDOW, synth.SHIFT, padded, device=DEV)
     reg = wgs.build_shift_regions(grid, synth.WINDOW, synth.SHIFT, padded, device=DEV)
@@ -123,21 +123,37 @@ def _block_library(x, w, grid, padded, heads):
     return out
 
 
+# (grid, padded, width) of the gate's blocks: the tiny grids, and the two
+# stages at full size (the 384 stage on its fully padded grid, as attention
+# needs equal windows)
+BLOCKS = {
+    "tiny": (synth.TINY.grid, synth.TINY.padded, 192),
+    "tiny_padded": (synth.TINY_PADDED.grid, synth.TINY_PADDED.padded, 192),
+    "c192": (synth.ATTN_192.grid, synth.ATTN_192.padded, 192),
+    "c384": (synth.ATTN_384.grid, synth.ATTN_384.padded, 384),
+}
+# max / mean bounds per format, about 4x what GB300 measured (fp16: max
+# 4.4e-3, mean 5e-4 on the tiny grids, outputs of magnitude ~1)
+BOUNDS = {torch.float16: (0.02, 2e-3), torch.bfloat16: (0.16, 1.6e-2)}
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("stage", [synth.TINY, synth.TINY_PADDED], ids=lambda s: s.name)
-def test_one_block_against_a_float32_torch_block(stage):
-    heads = stage.width // 32
-    x, _ = synth.residual_branch(stage.tokens, stage.width, seed=12)
-    w = _weights(stage.width, heads, seed=13)
-    ref = _block_reference(x.to(DEV).float(), w, stage.grid, stage.padded, heads)
-    got = _block_library(x.to(DEV), w, stage.grid, stage.padded, heads).float()
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("name", sorted(BLOCKS))
+def test_one_block_against_a_float32_torch_block(name, dtype):
+    grid, padded, width = BLOCKS[name]
+    heads = width // 32
+    tokens = grid[0] * grid[1] * grid[2]
+    x, _ = synth.residual_branch(tokens, width, seed=12)
+    w = _weights(width, heads, seed=13)
+    ref = _block_reference(x.to(DEV).float(), w, grid, padded, heads)
+    got = _block_library(x.to(DEV).to(dtype), w, grid, padded, heads, dtype).float()
     err = (got - ref).abs()
     scale = ref.abs().mean().item()
-    # an fp16 pipeline against float32, outputs of magnitude ~1: measured
-    # max 4.4e-3 and mean 5e-4 on GB300 (a few fp16 ulps); bounds at ~4x that
-    assert err.max().item() < 0.02, (err.max().item(), scale)
-    assert err.mean().item() < 2e-3, (err.mean().item(), scale)
-    print(stage.name, "max", err.max().item(), "mean", err.mean().item(), "scale", scale)
+    print(name, dtype, "max", err.max().item(), "mean", err.mean().item(), "scale", scale)
+    bmax, bmean = BOUNDS[dtype]
+    assert err.max().item() < bmax, (err.max().item(), scale)
+    assert err.mean().item() < bmean, (err.mean().item(), scale)
 
 
 def test_the_torch_window_helpers_match_the_library_maps():
