@@ -36,33 +36,33 @@ def _weights(c, heads, seed):
     return {k: v.to(DEV) for k, v in w.items()}
 
 
-def _windows_torch(t, grid, padded):
+def _windows_torch(t, grid, padded, shift=synth.SHIFT):
     """[Z*H*W, C] -> [n_win, n, C]: roll by -shift, zero-pad at the high end,
     window-major partition, row-major inside a window."""
     (Z, H, W), (wz, wh, ww) = grid, synth.WINDOW
     c = t.shape[-1]
-    x = t.view(Z, H, W, c).roll(shifts=tuple(-s for s in synth.SHIFT), dims=(0, 1, 2))
+    x = t.view(Z, H, W, c).roll(shifts=tuple(-s for s in shift), dims=(0, 1, 2))
     x = torch.nn.functional.pad(x, (0, 0, 0, padded[2] - W, 0, padded[1] - H, 0, padded[0] - Z))
     x = x.view(padded[0] // wz, wz, padded[1] // wh, wh, padded[2] // ww, ww, c)
     return x.permute(0, 2, 4, 1, 3, 5, 6).reshape(-1, wz * wh * ww, c)
 
 
-def _unwindows_torch(w, grid, padded):
+def _unwindows_torch(w, grid, padded, shift=synth.SHIFT):
     (Z, H, W), (wz, wh, ww) = grid, synth.WINDOW
     c = w.shape[-1]
     x = w.view(padded[0] // wz, padded[1] // wh, padded[2] // ww, wz, wh, ww, c)
     x = x.permute(0, 3, 1, 4, 2, 5, 6).reshape(*padded, c)[:Z, :H, :W]
-    return x.roll(shifts=synth.SHIFT, dims=(0, 1, 2)).reshape(Z * H * W, c)
+    return x.roll(shifts=tuple(shift), dims=(0, 1, 2)).reshape(Z * H * W, c)
 
 
-def _labels_torch(grid, padded):
+def _labels_torch(grid, padded, shift=synth.SHIFT):
     """Region label of every padded cell from its coordinates (the reading of
     the shift mask: bit k when the cell lies past the roll's seam along k),
     laid out like the windows."""
     coords = torch.meshgrid(*(torch.arange(p) for p in padded), indexing="ij")
     lab = torch.zeros(padded, dtype=torch.int64)
     for k in range(3):
-        s = synth.SHIFT[k] % grid[k]
+        s = shift[k] % grid[k]
         if s:
             lab += ((coords[k] + s) >= grid[k]).long() << k
     return _windows_torch_cells(lab, padded)
@@ -170,3 +170,74 @@ def test_the_torch_window_helpers_match_the_library_maps():
         lab = _labels_torch(stage.grid, stage.padded).reshape(-1).numpy()
         ours = wgs.build_shift_regions(stage.grid, synth.WINDOW, synth.SHIFT, stage.padded)
         assert np.array_equal(lab, ours.numpy())
+
+
+def _two_blocks_reference(x, w1, w2, grid, padded, heads):
+    """Float32 torch: an unshifted block, then a shifted one (Swin's pair)."""
+    c = x.shape[1]
+
+    def block(x, w, shift):
+        w = {k: v.float() for k, v in w.items()}
+        h = _windows_torch(torch.nn.functional.layer_norm(x, (c,), eps=EPS), grid, padded, shift)
+        lab = _labels_torch(grid, padded, shift).to(x.device)
+        mask = torch.where(lab[:, :, None] == lab[:, None, :], 0.0, -100.0)[:, None]
+        a = _attention(h, w, heads, lambda s: s + w["pos"] + mask)
+        r = x + _unwindows_torch(a, grid, padded, shift)
+        m = torch.nn.functional.layer_norm(r, (c,), eps=EPS) @ w["fc1"]
+        return r + torch.nn.functional.gelu(m + w["fc1_b"], approximate="tanh") @ w["fc2"] + w["fc2_b"]
+
+    return block(block(x, w1, (0, 0, 0)), w2, synth.SHIFT)
+
+
+def _two_blocks_library(x, w1, w2, grid, padded, heads, dtype):
+    """The same pair in x's format.  The block boundary is one
+    residual_add_norm_gather: block 1's residual stream + its MLP output,
+    written out, normalised by block 2's norm1 and gathered into block 2's
+    shifted windows."""
+    c = x.shape[1]
+    n = synth.WINDOW[0] * synth.WINDOW[1] * synth.WINDOW[2]
+    maps = {}
+    for tag, shift in (("a", (0, 0, 0)), ("b", synth.SHIFT)):
+        maps[tag] = (wgs.build_window_index(grid, synth.WINDOW, shift, padded, device=DEV),
+                     wgs.build_window_inverse(grid, synth.WINDOW, shift, padded, device=DEV),
+                     wgs.build_shift_regions(grid, synth.WINDOW, shift, padded, device=DEV))
+
+    def attention_and_mlp(resid, windows, w, tag, masked):
+        w = {k: v.to(dtype) for k, v in w.items()}
+        _, inv, reg = maps[tag]
+
+        def mask_add(s):
+            return wgs.window_bias_mask_add(s.contiguous(), w["pos"], None,
+                                            reg if masked else None, -100.0)
+
+        a = _attention(windows.view(-1, n, c), w, heads, mask_add).reshape(-1, c)
+        r, y = wgs.window_reverse_add_ln_fwd(resid, a, inv, EPS)
+        m = wgs.bias_gelu_tanh((y @ w["fc1"]).contiguous(), w["fc1_b"])
+        return r, (m @ w["fc2"] + w["fc2_b"]).contiguous()
+
+    r1, mlp1 = attention_and_mlp(x, wgs.norm_gather(x, maps["a"][0], EPS), w1, "a", False)
+    r2_in, windows2 = wgs.residual_add_norm_gather(r1, mlp1, maps["b"][0], EPS)
+    r2, mlp2 = attention_and_mlp(r2_in, windows2, w2, "b", True)
+    wgs.check_error(DEV)
+    return r2 + mlp2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("name", ["tiny_padded", "c192", "c384"])
+def test_two_blocks_with_the_fused_block_boundary(name, dtype):
+    """Every op of the path in one sequence: norm1 + gather, bias-mask,
+    reverse + add + norm2, bias + GELU, then the fused residual add + norm1
+    + gather into the next, shifted block."""
+    grid, padded, width = BLOCKS[name]
+    heads = width // 32
+    tokens = grid[0] * grid[1] * grid[2]
+    x, _ = synth.residual_branch(tokens, width, seed=14)
+    w1, w2 = _weights(width, heads, seed=15), _weights(width, heads, seed=16)
+    ref = _two_blocks_reference(x.to(DEV).float(), w1, w2, grid, padded, heads)
+    got = _two_blocks_library(x.to(DEV).to(dtype), w1, w2, grid, padded, heads, dtype).float()
+    err = (got - ref).abs()
+    print(name, dtype, "two blocks: max", err.max().item(), "mean", err.mean().item(),
+          "scale", ref.abs().mean().item())
+    bmax, bmean = BOUNDS[dtype]
+    assert err.max().item() < 2 * bmax and err.mean().item() < 2 * bmean
