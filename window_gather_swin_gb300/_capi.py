@@ -69,6 +69,8 @@ def lib_path() -> str:
 def load(path: str | None = None):
     """Load libwgs.so (building it first if nvcc is present and it is stale)."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib

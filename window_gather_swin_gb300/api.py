@@ -45,17 +45,36 @@ def _cuda(t: torch.Tensor, name: str, dtype=None) -> None:
 
 
 def _same_device(*ts: torch.Tensor) -> None:
-    dev = ts[0].device
+    dev = ts[0].get_device()
     for t in ts[1:]:
-        _require(t.device == dev, f"all tensors must be on {dev} (got {t.device})")
+        _require(t.get_device() == dev, f"all tensors must be on {ts[0].device} (got {t.device})")
 
 
 def _stream_ptr(device: torch.device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
-    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
+try:  # the current stream's raw handle, without building a Stream object
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+except AttributeError:  # pragma: no cover
+    def _raw_stream(index):
+        return torch.cuda.current_stream(index).cuda_stream
+
+
+def _call(name: str, fn, device: torch.device, *args) -> None:
+    """fn(*args, stream) with `device`'s current stream, raising on a non-OK
+    status; the device is made current only when it is not already."""
+    index = device.index
+    if torch.cuda.current_device() == index:
+        _capi.check(name, fn(*args, _raw_stream(index)))
+    else:
+        with torch.cuda.device(index):
+            _capi.check(name, fn(*args, _raw_stream(index)))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    """Device address of t, or 0 (NULL) for None or an empty tensor."""
+    return t.data_ptr() if t is not None and t.numel() > 0 else 0
 
 
 def _out(out: Optional[torch.Tensor], like_shape, dtype, device, name: str) -> torch.Tensor:
@@ -83,9 +102,8 @@ def ln_fwd(x: torch.Tensor, eps: float = 1e-5, out: Optional[torch.Tensor] = Non
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
     y = _out(out, x.shape, x.dtype, x.device, "out")
     _same_device(x, y)
-    with torch.cuda.device(x.device):
-        _capi.check("ln_fwd", _entry("ln_fwd", x.dtype)(_ptr(x), _ptr(y), rows, width, float(eps),
-                                                        _stream_ptr(x.device)))
+    _call("ln_fwd", _entry("ln_fwd", x.dtype), x.device, _ptr(x), _ptr(y), rows, width,
+          float(eps))
     return y
 
 
@@ -103,10 +121,8 @@ def residual_add_ln_fwd(residual: torch.Tensor, branch: torch.Tensor, eps: float
     r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
     y = _out(out, residual.shape, residual.dtype, residual.device, "out")
     _same_device(residual, branch, r, y)
-    with torch.cuda.device(residual.device):
-        _capi.check("residual_add_ln_fwd", _entry("residual_add_ln_fwd", residual.dtype)(
-            _ptr(residual), _ptr(branch), _ptr(r), _ptr(y), rows, width, float(eps),
-            _stream_ptr(residual.device)))
+    _call("residual_add_ln_fwd", _entry("residual_add_ln_fwd", residual.dtype), residual.device,
+          _ptr(residual), _ptr(branch), _ptr(r), _ptr(y), rows, width, float(eps))
     return r, y
 
 
@@ -128,9 +144,8 @@ def window_gather(src: torch.Tensor, idx: torch.Tensor,
     """dst[d] = src[idx[d]] (idx >= 0) or a zero row (idx == -1).  Rows are
     copied bit for bit, so fp16 and bfloat16 use the same kernel."""
     n_src, width, dst = _gather_args(src, idx, out, "window_gather")
-    with torch.cuda.device(src.device):
-        _capi.check("window_gather", _capi.load().window_gather(
-            _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, _stream_ptr(src.device)))
+    _call("window_gather", _capi.load().window_gather, src.device,
+          _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width)
     return dst
 
 
@@ -139,10 +154,8 @@ def norm_gather(src: torch.Tensor, idx: torch.Tensor, eps: float = 1e-5,
     """dst[d] = LN(src[idx[d]]) (idx >= 0) or a zero row (idx == -1)."""
     n_src, width, dst = _gather_args(src, idx, out, "norm_gather")
     _require(width in LN_WIDTHS, f"width must be one of {LN_WIDTHS} (got {width})")
-    with torch.cuda.device(src.device):
-        _capi.check("norm_gather", _entry("norm_gather", src.dtype)(
-            _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, float(eps),
-            _stream_ptr(src.device)))
+    _call("norm_gather", _entry("norm_gather", src.dtype), src.device,
+          _ptr(src), _ptr(idx), _ptr(dst), n_src, idx.numel(), width, float(eps))
     return dst
 
 
@@ -165,10 +178,9 @@ def window_reverse_add_ln_fwd(residual: torch.Tensor, windows: torch.Tensor,
     r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
     y = _out(out, residual.shape, residual.dtype, residual.device, "out")
     _same_device(residual, windows, inv_idx, r, y)
-    with torch.cuda.device(residual.device):
-        _capi.check("window_reverse_add_ln_fwd", _entry("window_reverse_add_ln_fwd", residual.dtype)(
-            _ptr(residual), _ptr(windows), _ptr(inv_idx), _ptr(r), _ptr(y), rows,
-            windows.shape[0], width, float(eps), _stream_ptr(residual.device)))
+    _call("window_reverse_add_ln_fwd", _entry("window_reverse_add_ln_fwd", residual.dtype),
+          residual.device, _ptr(residual), _ptr(windows), _ptr(inv_idx), _ptr(r), _ptr(y), rows,
+          windows.shape[0], width, float(eps))
     return r, y
 
 
@@ -188,10 +200,9 @@ def residual_add_norm_gather(residual: torch.Tensor, branch: torch.Tensor, idx: 
     r = _out(residual_out, residual.shape, residual.dtype, residual.device, "residual_out")
     dst = _out(out, (idx.numel(), width), residual.dtype, residual.device, "out")
     _same_device(residual, branch, idx, r, dst)
-    with torch.cuda.device(residual.device):
-        _capi.check("residual_add_norm_gather", _entry("residual_add_norm_gather", residual.dtype)(
-            _ptr(residual), _ptr(branch), _ptr(idx), _ptr(r), _ptr(dst), n_src, idx.numel(), width,
-            float(eps), _stream_ptr(residual.device)))
+    _call("residual_add_norm_gather", _entry("residual_add_norm_gather", residual.dtype),
+          residual.device, _ptr(residual), _ptr(branch), _ptr(idx), _ptr(r), _ptr(dst), n_src,
+          idx.numel(), width, float(eps))
     return r, dst
 
 
@@ -210,9 +221,8 @@ def bias_gelu_tanh(x: torch.Tensor, bias: torch.Tensor,
     rows = x.numel() // width if width else 0
     y = _out(out, x.shape, x.dtype, x.device, "out")
     _same_device(x, bias, y)
-    with torch.cuda.device(x.device):
-        _capi.check("bias_gelu_tanh", _capi.load().bias_gelu_tanh(
-            _ptr(x), _ptr(bias), _ptr(y), rows, width, _DTYPE[x.dtype], _stream_ptr(x.device)))
+    _call("bias_gelu_tanh", _capi.load().bias_gelu_tanh, x.device,
+          _ptr(x), _ptr(bias), _ptr(y), rows, width, _DTYPE[x.dtype])
     return y
 
 
@@ -246,10 +256,9 @@ def bias_gelu_tanh_bwd(grad_y: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _cuda(workspace, "workspace", torch.uint8)
     _same_device(grad_y, x, bias, gx, gb, workspace)
-    with torch.cuda.device(x.device):
-        _capi.check("bias_gelu_tanh_bwd", lib.bias_gelu_tanh_bwd(
-            _ptr(grad_y), _ptr(x), _ptr(bias), _ptr(gx), _ptr(gb), _ptr(workspace),
-            workspace.numel(), rows, width, _DTYPE[x.dtype], _stream_ptr(x.device)))
+    _call("bias_gelu_tanh_bwd", lib.bias_gelu_tanh_bwd, x.device,
+          _ptr(grad_y), _ptr(x), _ptr(bias), _ptr(gx), _ptr(gb), _ptr(workspace),
+          workspace.numel(), rows, width, _DTYPE[x.dtype])
     return gx, gb
 
 
@@ -280,10 +289,9 @@ def window_bias_mask_add(scores: torch.Tensor, bias: torch.Tensor,
         ts.append(region)
     y = _out(out, scores.shape, scores.dtype, scores.device, "out")
     _same_device(*ts, y)
-    with torch.cuda.device(scores.device):
-        _capi.check("window_bias_mask_add", _capi.load().window_bias_mask_add(
-            _ptr(scores), _ptr(bias), _ptr(win_type), _ptr(region), _ptr(y), n_win, heads, n,
-            n_types, float(mask_value), _DTYPE[scores.dtype], _stream_ptr(scores.device)))
+    _call("window_bias_mask_add", _capi.load().window_bias_mask_add, scores.device,
+          _ptr(scores), _ptr(bias), _ptr(win_type), _ptr(region), _ptr(y), n_win, heads, n,
+          n_types, float(mask_value), _DTYPE[scores.dtype])
     return y
 
 
