@@ -546,6 +546,24 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def test_fp16_residual_add_every_pattern():
+    """r = fp16(a + b) bit for bit on every binary16 pattern as a (subnormals,
+    signed zeros, infinities, NaN) against shuffled partners."""
+    rng = np.random.default_rng(8)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    n = -(-pats.size // 192) * 192
+    a = np.resize(pats, n).view(np.float16).reshape(-1, 192)
+    b = rng.permutation(np.resize(pats, n)).view(np.float16).reshape(-1, 192)
+    r, _ = wgs.residual_add_ln_fwd(torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV), EPS)
+    o_r, _ = oracle.residual_add_ln(a, b, EPS)
+    g = np_(r).view(np.uint16).ravel()
+    w = o_r.view(np.uint16).ravel()
+    nan = lambda v: ((v & 0x7C00) == 0x7C00) & ((v & 0x3FF) != 0)  # noqa: E731
+    assert np.array_equal(nan(g), nan(w))
+    ok = ~nan(w)
+    assert np.array_equal(g[ok], w[ok]), np.flatnonzero(g[ok] != w[ok])[:5]
+
+
 def test_bf16_residual_add_every_pattern():
     """The residual sum r = bf16(a + b) bit for bit on every bf16 pattern as
     a (subnormals, signed zeros, infinities, NaN) against shuffled b, and on

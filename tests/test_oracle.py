@@ -150,6 +150,30 @@ def test_residual_sum_is_fp16_of_fp32_sum():
     assert np.array_equal(r.view(np.uint16), want.view(np.uint16))
 
 
+def test_residual_sum_exhaustive_over_b_for_chosen_a():
+    """Every finite binary16 b against 80 chosen a (signed zeros, the
+    smallest and largest subnormals and normals, a value at and one between
+    every power of two from 2^-14 to 2^15, the largest finite, odd
+    mantissas): 5.2 M pairs, all exact against numpy's widen-add-round."""
+    every = _all_f16()
+    picks = [0.0, -0.0, 6e-8, -6e-8, 6.1e-5, -6.1e-5, 65504.0, -65504.0]
+    for e in range(-14, 16):
+        picks += [2.0 ** e, -(2.0 ** e) * 1.5]
+    picks += [0.1, -0.3, 1.0009765625, 3.14, 1000.5, -2049.0, 0.33325, -7.998]
+    picks += [1.0 - 2 ** -11, 2049.0, 4097.0, -8191.0]
+    a_vals = np.array(picks, dtype=np.float16)
+    assert a_vals.size == 80
+    fin_b = every[np.isfinite(every.astype(np.float64))]
+    n = (fin_b.size // 192) * 192
+    b = fin_b[:n].reshape(-1, 192)
+    for av in a_vals:
+        a = np.full_like(b, av)
+        r, _ = oracle.residual_add_ln(a, b, EPS)
+        with np.errstate(over="ignore", invalid="ignore"):
+            want = a + b
+        assert np.array_equal(r.view(np.uint16), want.view(np.uint16)), float(av)
+
+
 def test_residual_ln_is_taken_after_the_fp16_rounding():
     a, b = synth.residual_branch(576, 192, seed=0)
     a, b = a.numpy(), b.numpy()
