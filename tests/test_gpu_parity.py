@@ -895,3 +895,68 @@ def test_bias_mask_bad_window_type_sets_error_word():
     want = oracle.window_bias_mask_add(np_(s)[:2], np_(b), types[:2], None)
     _check_bias_mask(out[:2], want, "f16", "good windows")
     wgs.check_error(DEV)                                         # cleared
+
+
+# ----------------------------------------------------------- seeded fuzz ----
+
+@pytest.mark.parametrize("seed", range(32))
+def test_seeded_fuzz_of_every_op(seed):
+    """Random grids, shifts (either order), row counts, widths and formats
+    for every op, each against the oracle with the rules above."""
+    from parity import LN_TIE_ABS, check_bf16_near
+    rng = np.random.default_rng(1000 + seed)
+    fmt = ["f16", "bf16"][seed % 2]
+    dt = torch.float16 if fmt == "f16" else torch.bfloat16
+    width = [192, 384][(seed // 2) % 2]
+    grid = tuple(int(v) for v in rng.integers(1, [5, 20, 30]))
+    win = tuple(int(v) for v in rng.integers(1, [3, 7, 13]))
+    shift = tuple(int(v) for v in rng.integers(-15, 16, 3))
+    flags = int(rng.integers(0, 2))
+    n_tok = grid[0] * grid[1] * grid[2]
+
+    def near(gpu_t, o16, y64, what):
+        if fmt == "f16":
+            check_ln(np_(gpu_t), o16, y64, what)
+        else:
+            check_bf16_near(_bits(gpu_t), o16, y64, what, tie_abs=LN_TIE_ABS)
+
+    to_o = (lambda t: t.numpy()) if fmt == "f16" else _bits
+    a, b = synth.residual_branch(n_tok, width, seed=seed, dtype=dt)
+    idx = wgs.build_window_index(grid, win, shift, None, flags)
+    om = oracle.build_window_index(grid, win, shift, None, flags)
+    assert np.array_equal(idx.numpy(), om)
+    r, g = wgs.residual_add_norm_gather(a.to(DEV), b.to(DEV), idx.to(DEV), EPS)
+    o_r, o_g, bad = oracle.residual_add_norm_gather(to_o(a), to_o(b), om, EPS, fmt=fmt)
+    assert bad == 0 and np.array_equal(_bits(r), o_r.view(np.uint16))
+    y64 = oracle.ln_f64(o_r, EPS, fmt=fmt)
+    near(g, o_g, np.where((om >= 0)[:, None], y64[np.maximum(om, 0)], 0.0), "fuzz add+norm+gather")
+
+    inv = wgs.build_window_inverse(grid, win, shift, None, flags)
+    windows = synth.gather_source(idx.numel(), width, seed=seed + 50, dtype=dt)
+    r2, y2 = wgs.window_reverse_add_ln_fwd(a.to(DEV), windows.to(DEV), inv.to(DEV), EPS)
+    o_r2, o_y2, bad = oracle.window_reverse_add_ln(to_o(a), to_o(windows), om, EPS, fmt=fmt)
+    assert bad == 0 and np.array_equal(_bits(r2), o_r2.view(np.uint16))
+    near(y2, o_y2, oracle.ln_f64(o_r2, EPS, fmt=fmt), "fuzz reverse+add+ln")
+
+    rows, gw = int(rng.integers(0, 3000)), int(rng.choice([8, 64, 768, 1000, 1536, 2056]))
+    x, bias = synth.gelu_input(rows, gw, dt, seed=seed + 70)
+    gy, _ = synth.gelu_input(rows, gw, dt, seed=seed + 71)
+    z = wgs.bias_gelu_tanh(x.to(DEV), bias.to(DEV))
+    o_z, z64 = oracle.bias_gelu_tanh(to_o(x), to_o(bias), fmt=fmt)
+    if rows:
+        if fmt == "f16":
+            check_fp16_near(np_(z), o_z, z64, "fuzz gelu")
+        else:
+            check_bf16_near(_bits(z), o_z, z64, "fuzz gelu")
+    gx, gb = wgs.bias_gelu_tanh_bwd(gy.to(DEV), x.to(DEV), bias.to(DEV))
+    _check_bwd(to_o(gy), to_o(x), to_o(bias), to_o(gx.cpu()), to_o(gb.cpu()), fmt, "fuzz bwd")
+
+    nw, heads, n = int(rng.integers(1, 9)), int(rng.integers(1, 5)), int(rng.choice([8, 24, 144, 12]))
+    sc, sb = synth.attention_logits(nw, heads, n, 2, seed=seed + 90, dtype=dt)
+    types = rng.integers(0, 2, nw).astype(np.int32)
+    reg = rng.integers(0, 3, nw * n).astype(np.int32)
+    bm = wgs.window_bias_mask_add(sc.to(DEV), sb.to(DEV), torch.from_numpy(types).to(DEV),
+                                  torch.from_numpy(reg).to(DEV), -100.0)
+    _check_bias_mask(bm, oracle.window_bias_mask_add(to_o(sc), to_o(sb), types, reg, -100.0,
+                                                     fmt=fmt), fmt, "fuzz bias-mask")
+    wgs.check_error(DEV)
