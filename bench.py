@@ -179,16 +179,36 @@ def build_next_calls():
         lambda i, o: wgs.residual_add_norm_gather(i["a"], i["b"], i["idx"], EPS,
                                                   residual_out=o["r"], out=o["dst"]),
         None, m))
+    calls.append(Call(
+        "residual_add_ln_fwd", f"bf16 [{n},{c}]", 8 * n * c, {"a": ab, "b": bb},
+        {"r": ((n, c), bf), "y": ((n, c), bf)},
+        lambda i, o: wgs.residual_add_ln_fwd(i["a"], i["b"], EPS, residual_out=o["r"], out=o["y"]),
+        None, n))
+    srcb = synth.gather_source(n, c, seed=3, dtype=bf)
+    calls.append(Call(
+        "norm_gather", f"bf16 [{n},{c}]->{m}", 2 * c * n + (2 * c + 4) * m,
+        {"src": srcb, "idx": idx}, {"dst": ((m, c), bf)},
+        lambda i, o: wgs.norm_gather(i["src"], i["idx"], EPS, out=o["dst"]), None, m))
+    invb = wgs.build_window_inverse(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+    winb = synth.gather_source(m, c, seed=3, dtype=bf)
+    calls.append(Call(
+        "window_reverse_add_ln_fwd", f"bf16 {m}->[{n},{c}]", 8 * n * c + 4 * n,
+        {"res": ab, "win": winb, "inv": invb}, {"r": ((n, c), bf), "y": ((n, c), bf)},
+        lambda i, o: wgs.window_reverse_add_ln_fwd(i["res"], i["win"], i["inv"], EPS,
+                                                   residual_out=o["r"], out=o["y"]),
+        None, n))
     rows, width = synth.GELU_F16_SHAPE
     xg, bg = synth.gelu_input(rows, width, bf, seed=4)
     # backward of bias + GELU (algorithmic bytes: grad_y and x read, grad_x
     # written, bias read and grad_bias written; the partial sums are extra)
-    for (r_, w_), dt_ in ((synth.GELU_F32_SHAPE, torch.float32), (synth.GELU_F16_SHAPE, torch.float16)):
+    for (r_, w_), dt_ in ((synth.GELU_F32_SHAPE, torch.float32), (synth.GELU_F16_SHAPE, torch.float16),
+                          (synth.GELU_F16_SHAPE, bf)):
         esz = 4 if dt_ == torch.float32 else 2
+        tag = {torch.float32: "fp32", torch.float16: "fp16", bf: "bf16"}[dt_]
         xg_, bg_ = synth.gelu_input(r_, w_, dt_, seed=4)
         gy_, _ = synth.gelu_input(r_, w_, dt_, seed=5)
         calls.append(Call(
-            "bias_gelu_tanh_bwd", f"{'fp32' if esz == 4 else 'fp16'} [{r_},{w_}]",
+            "bias_gelu_tanh_bwd", f"{tag} [{r_},{w_}]",
             3 * r_ * w_ * esz + 2 * w_ * esz, {"gy": gy_, "x": xg_, "bias": bg_},
             {"gx": ((r_, w_), dt_), "gb": ((w_,), dt_), "ws": ((wgs.gelu_bwd_workspace_bytes(r_, w_),), torch.uint8)},
             lambda i, o: wgs.bias_gelu_tanh_bwd(i["gy"], i["x"], i["bias"], grad_x=o["gx"],
@@ -199,13 +219,15 @@ def build_next_calls():
                       lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]), None, rows))
     # position bias + shift mask on the attention logits (algorithmic bytes:
     # logits read and written, the bias slab and the labels read once)
-    for ast in (synth.ATTN_192, synth.ATTN_384):
-        s_, b_ = synth.attention_logits(ast.n_win, ast.heads, ast.n, 1, seed=6)
+    for ast, dt_ in ((synth.ATTN_192, torch.float16), (synth.ATTN_384, torch.float16),
+                     (synth.ATTN_192, bf)):
+        s_, b_ = synth.attention_logits(ast.n_win, ast.heads, ast.n, 1, seed=6, dtype=dt_)
         reg = wgs.build_shift_regions(ast.grid, synth.WINDOW, synth.SHIFT, ast.padded)
+        tag = "fp16" if dt_ == torch.float16 else "bf16"
         calls.append(Call(
-            "window_bias_mask_add", f"fp16 [{ast.n_win},{ast.heads},{ast.n},{ast.n}]",
+            "window_bias_mask_add", f"{tag} [{ast.n_win},{ast.heads},{ast.n},{ast.n}]",
             4 * s_.numel() + 2 * b_.numel() + 4 * reg.numel(),
-            {"s": s_, "b": b_, "reg": reg}, {"out": (tuple(s_.shape), torch.float16)},
+            {"s": s_, "b": b_, "reg": reg}, {"out": (tuple(s_.shape), dt_)},
             lambda i, o: wgs.window_bias_mask_add(i["s"], i["b"], None, i["reg"], out=o["out"]),
             None, ast.n_win * ast.heads * ast.n))
     return calls
