@@ -14,16 +14,22 @@
 //
 // Layout: a logits row is n 16-bit elements = n/8 16-byte chunks.  A CTA of
 // RP x (n/8) threads gives every thread one fixed chunk column and RP rows
-// per pass, U passes in flight; the grid strides over blocks of RP x U rows
-// of the flattened [n_win x heads x n] row space.  A row's window, head and
-// query index come from two divisions by invariant integers done as
-// multiply-high (Granlund & Montgomery 1994).
+// per pass, U passes in flight.  The grid strides over units, each a
+// contiguous run of rows of one (window, head) tile: a tile's passes are
+// split into the fewest parts of at most WGS_BM_PART_PASSES passes, evened
+// out (n = 144, RP = 7, U = 2: 11 passes in parts of 56, 56 and 32 rows).
+// A unit's window and head come from two
+// divisions by invariant integers done as multiply-high (Granlund &
+// Montgomery 1994); its window type and column labels are loaded once.
 #include <atomic>
 
 #include "wgs_common.cuh"
 
 #ifndef WGS_BM_U
 #define WGS_BM_U 2  // rows in flight per thread
+#endif
+#ifndef WGS_BM_PART_PASSES
+#define WGS_BM_PART_PASSES 4  // passes of RP x U rows per unit, at most
 #endif
 #ifndef WGS_BM_THREADS
 #define WGS_BM_THREADS 128  // threads per CTA to aim for (vector path)
@@ -64,61 +70,68 @@ __device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t
     return (c_lo != row ? (mask2 & 0xffffu) : 0u) | (c_hi != row ? (mask2 & 0xffff0000u) : 0u);
 }
 
+// The grid strides over units: one (window, head) tile's rows
+// [part * part_rows, (part + 1) * part_rows).  A unit's window type, column
+// labels and base addresses are found once; its rows then stream with plain
+// offsets, U passes of RP rows in flight.
 template <typename E, int U>
 __global__ void __launch_bounds__(kMaxChunksPerRow > WGS_BM_THREADS ? kMaxChunksPerRow : WGS_BM_THREADS)
 bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
-              const int32_t *region, uint4 *out, unsigned int *err, uint32_t rows, int32_t n,
-              int32_t heads, int32_t n_types, int32_t cpr, int32_t rp, FastDiv by_n,
-              FastDiv by_heads, uint32_t mask2) {
+                const int32_t *region, uint4 *out, unsigned int *err, uint32_t units, int32_t n,
+                int32_t heads, int32_t n_types, int32_t cpr, int32_t rp, int32_t part_rows,
+                int32_t parts, FastDiv by_parts, FastDiv by_heads, uint32_t mask2) {
     pdl_prologue();
     const int jc = static_cast<int>(threadIdx.x) % cpr, lr = static_cast<int>(threadIdx.x) / cpr;
-    if (lr >= rp) return;  // no barrier below, so spare threads may leave
-    const uint32_t block = static_cast<uint32_t>(rp) * U;
-    for (uint32_t base = blockIdx.x * block; base < rows; base += gridDim.x * block) {
-        uint4 sv[U], bv[U];
-        int4 c0[U], c1[U];
-        int32_t li[U];
-        bool ok[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t r = base + lr + u * rp;
-            ok[u] = false;
-            if (r < rows) {
-                const uint32_t tile = div_by(r, by_n), i = r - tile * n;
-                const uint32_t w = div_by(tile, by_heads), h = tile - w * heads;
-                const int32_t type = win_type ? __ldg(win_type + w) : 0;
-                ok[u] = type >= 0 && type < n_types;
-                sv[u] = ld_stream(scores + static_cast<int64_t>(r) * cpr + jc);
-                if (ok[u])
-                    bv[u] = __ldg(bias + ((static_cast<int64_t>(type) * heads + h) * n + i) * cpr + jc);
-                if (region) {
-                    const int32_t *lab = region + static_cast<int64_t>(w) * n;
-                    li[u] = __ldg(lab + i);
-                    c0[u] = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc);
-                    c1[u] = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc + 1);
-                }
-            }
+    if (lr >= rp) return;
+    for (uint32_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const uint32_t tile = div_by(unit, by_parts);
+        const int32_t part = static_cast<int32_t>(unit - tile * static_cast<uint32_t>(parts));
+        const uint32_t w = div_by(tile, by_heads), h = tile - w * heads;
+        const int32_t type = win_type ? __ldg(win_type + w) : 0;
+        const bool ok = type >= 0 && type < n_types;
+        const int32_t *lab = region + static_cast<int64_t>(w) * n;
+        int4 c0 = make_int4(0, 0, 0, 0), c1 = c0;
+        if (region) {
+            c0 = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc);
+            c1 = __ldg(reinterpret_cast<const int4 *>(lab) + 2 * jc + 1);
         }
+        const int32_t i1 = (part + 1) * part_rows < n ? (part + 1) * part_rows : n;
+        const uint4 *sp = scores + static_cast<int64_t>(tile) * n * cpr + jc;
+        const uint4 *bp = bias + (static_cast<int64_t>(ok ? type : 0) * heads + h) * n * cpr + jc;
+        uint4 *op = out + static_cast<int64_t>(tile) * n * cpr + jc;
+        for (int32_t i = part * part_rows + lr; i < i1; i += rp * U) {
+            uint4 sv[U], bv[U];
+            int32_t li[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t r = base + lr + u * rp;
-            if (r >= rows) continue;
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
-            if (ok[u]) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t t = E::add2(word(sv[u], k), word(bv[u], k));
-                    if (region) {
-                        const int4 &c = k < 2 ? c0[u] : c1[u];
-                        const int32_t lo = (k & 1) ? c.z : c.x, hi = (k & 1) ? c.w : c.y;
-                        t = E::add2(t, mask_word(li[u], lo, hi, mask2));
-                    }
-                    set_word(o, k, t);
+            for (int u = 0; u < U; ++u) {
+                const int32_t ii = i + u * rp;
+                if (ii < i1) {
+                    sv[u] = ld_stream(sp + static_cast<int64_t>(ii) * cpr);
+                    if (ok) bv[u] = __ldg(bp + static_cast<int64_t>(ii) * cpr);
+                    if (region) li[u] = __ldg(lab + ii);
                 }
-            } else {
-                atomicOr(err, 1u);
             }
-            st_stream(out + static_cast<int64_t>(r) * cpr + jc, o);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t ii = i + u * rp;
+                if (ii >= i1) continue;
+                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                if (ok) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t t = E::add2(word(sv[u], k), word(bv[u], k));
+                        if (region) {
+                            const int4 &c = k < 2 ? c0 : c1;
+                            const int32_t lo = (k & 1) ? c.z : c.x, hi = (k & 1) ? c.w : c.y;
+                            t = E::add2(t, mask_word(li[u], lo, hi, mask2));
+                        }
+                        set_word(o, k, t);
+                    }
+                } else {
+                    atomicOr(err, 1u);
+                }
+                st_stream(op + static_cast<int64_t>(ii) * cpr, o);
+            }
         }
     }
 }
@@ -178,14 +191,20 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
             resident[dev.device].store((static_cast<int64_t>(threads) << 32) | per_sm,
                                        std::memory_order_relaxed);
         }
-        const int64_t blocks = ceil_div(rows, static_cast<int64_t>(rp) * U);
+        // the fewest parts of at most WGS_BM_PART_PASSES passes, evened out
+        const int32_t passes = static_cast<int32_t>(ceil_div(n, rp * U));
+        const int32_t part_passes = static_cast<int32_t>(
+            ceil_div(passes, ceil_div(passes, WGS_BM_PART_PASSES)));
+        const int32_t part_rows = part_passes * rp * U;
+        const int32_t parts = static_cast<int32_t>(ceil_div(n, part_rows));
+        const int64_t units = n_win * heads * parts;
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
-        return launch(kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)),
+        return launch(kernel, dim3(static_cast<unsigned>(units < cap ? units : cap)),
                       dim3(static_cast<unsigned>(rp * cpr)), 0, stream,
                       static_cast<const uint4 *>(scores), static_cast<const uint4 *>(bias),
                       win_type, region, static_cast<uint4 *>(out), err,
-                      static_cast<uint32_t>(rows), n, heads, n_types, cpr, rp,
-                      make_fastdiv(static_cast<uint32_t>(n)),
+                      static_cast<uint32_t>(units), n, heads, n_types, cpr, rp, part_rows, parts,
+                      make_fastdiv(static_cast<uint32_t>(parts)),
                       make_fastdiv(static_cast<uint32_t>(heads)), mask2);
     }
     const int64_t total = rows * n;
