@@ -594,7 +594,8 @@ def run_isolated(calls, dev, l2, peak, launches):
         sets = device_sets([c], dev, n_sets)
         g = capture(lambda: [c.run(sets[s % n_sets][0][0], sets[s % n_sets][1][0])
                              for s in range(per_graph)], dev)
-        g.replay()
+        for _ in range(3):  # warm-up: clocks and caches settle before timing
+            g.replay()
         # an event between replays: the per-call time of every replay gives
         # the spread (median, min, p90) besides the overall mean
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
