@@ -837,11 +837,14 @@ def test_bias_mask_full_size(st, per_type, axes, dtype, fmt):
 
 @pytest.mark.parametrize("fmt,dtype", [("f16", torch.float16), ("bf16", torch.bfloat16)])
 @pytest.mark.parametrize("n_win,heads,n", [(1, 1, 8), (5, 3, 16), (37, 2, 24), (3, 1, 2048),
+                                           (4, 3, 152), (3, 2, 296),
                                            (7, 2, 12), (2, 3, 6), (1, 1, 1)])
 @pytest.mark.parametrize("masked", [True, False])
 def test_bias_mask_sizes_and_paths(n_win, heads, n, masked, fmt, dtype):
     """Vector path (n % 8 == 0) and scalar path, ragged row blocks, window
-    types, labels and in-place use."""
+    types, labels and in-place use.  n = 152 and 296 split each (window,
+    head) tile into runs of rows whose last one is short (48/48/48/8 and
+    twelve of 24 then 8)."""
     rng = np.random.default_rng(n_win * 1000 + n)
     n_types = 3
     s, b = synth.attention_logits(n_win, heads, n, n_types, seed=n + heads, dtype=dtype)
