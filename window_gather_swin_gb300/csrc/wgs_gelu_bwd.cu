@@ -42,13 +42,17 @@
 #define WGS_BWD_GROUPS 4  // most row groups per CTA
 #endif
 #ifndef WGS_BWD_TARGET_THREADS
-#define WGS_BWD_TARGET_THREADS 98304  // pass-1 threads to aim for when choosing row groups
+// pass-1 threads to aim for when choosing row groups: two 384-thread CTAs on
+// each of 152 SMs, all that stay resident at the 80-register cap
+#define WGS_BWD_TARGET_THREADS 116736
 #endif
 #ifndef WGS_BWD_MIN_BLOCKS
 #define WGS_BWD_MIN_BLOCKS 2  // pass-1 CTAs of the largest size kept resident per SM
 #endif
 #ifndef WGS_BWD_MIN_SLAB_ROWS
-#define WGS_BWD_MIN_SLAB_ROWS 128  // rows per slab at least (slab count = min(512, rows / this))
+// slab count = min(512, ceil(rows / this)): 32760 rows give 304 slabs, which
+// with two row groups fill the resident CTA slots exactly
+#define WGS_BWD_MIN_SLAB_ROWS 108
 #endif
 
 namespace wgs {
