@@ -22,8 +22,10 @@
 // N(0,1) tensor) are recomputed from the same formula in FP64.
 //
 // The op streams 2 x rows x width elements through HBM; the vector path
-// moves 16-byte chunks and keeps U independent chunks in flight per thread.
-// Bias chunks come through L1 (the whole bias row is at most a few KB).
+// moves 16-byte chunks.  Rows of at least 64 chunks run as short CTAs of R
+// rows x one column block, a thread per column chunk; narrower rows run a
+// one-wave grid-stride kernel with U chunks in flight per thread.  Bias
+// chunks come through L1 (the whole bias row is at most a few KB).
 #include <atomic>
 #include <type_traits>
 
@@ -37,6 +39,12 @@
 #endif
 #ifndef WGS_GELU_U16
 #define WGS_GELU_U16 2  // chunks per thread per pass for 16-bit data, with prefetch
+#endif
+#ifndef WGS_GELU_R16
+#define WGS_GELU_R16 4  // rows per thread in the row-block form, 16-bit data
+#endif
+#ifndef WGS_GELU_R32
+#define WGS_GELU_R32 4  // rows per thread in the row-block form, fp32
 #endif
 #ifndef WGS_GELU_CTAS_PER_SM
 #define WGS_GELU_CTAS_PER_SM 0  // grid cap in CTAs per SM; 0: as many as can be resident
@@ -216,6 +224,31 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
     }
 }
 
+// Row-block form, for rows of at least kRowFormMinVecs chunks: CTA (row
+// block, column block); thread j owns column chunk blockIdx.y * cv + j of R
+// consecutive rows, with its bias chunk loaded once and the R chunks in
+// flight together.  The grid holds many short CTAs, so the hardware keeps
+// every SM fed as CTAs finish, with no index division anywhere.
+constexpr int32_t kRowFormMinVecs = 64;
+
+template <typename E, int R>
+__global__ void __launch_bounds__(256)
+bias_gelu_rows_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
+                      int32_t row_vecs, int32_t cv) {
+    pdl_prologue();
+    const int32_t c = static_cast<int32_t>(blockIdx.y) * cv + static_cast<int32_t>(threadIdx.x);
+    if (c >= row_vecs) return;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
+    const uint4 bv = __ldg(bias + c);
+    uint4 xv[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+        if (r0 + q < rows) xv[q] = ld_stream(x + (r0 + q) * row_vecs + c);
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+        if (r0 + q < rows) st_stream(y + (r0 + q) * row_vecs + c, gelu_chunk<E>(xv[q], bv));
+}
+
 // Any width, any element alignment: one element per thread per step.
 template <typename E>
 __global__ void __launch_bounds__(256)
@@ -245,10 +278,21 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
     const int64_t n = rows * width;
     const bool vec = width % kVec == 0 && aligned16(x) && aligned16(bias) && aligned16(y);
     if (vec) {
-        // 16-bit data: fewer chunks per pass, the next pass's loads issued
-        // before this pass computes (eight elements a chunk make the compute
-        // long enough to hide behind them); fp32: more chunks, no prefetch
         constexpr bool PF = !std::is_same<E, F32>::value;
+        constexpr int R = PF ? WGS_GELU_R16 : WGS_GELU_R32;
+        const int32_t row_vecs = static_cast<int32_t>(width / kVec);
+        if (row_vecs >= kRowFormMinVecs && ceil_div(rows, static_cast<int64_t>(R)) <= INT32_MAX) {
+            const int32_t cv = row_vecs <= 256 ? row_vecs : 256;
+            const dim3 grid(static_cast<unsigned>(ceil_div(rows, static_cast<int64_t>(R))),
+                            static_cast<unsigned>(ceil_div(row_vecs, cv)));
+            return launch(bias_gelu_rows_kernel<E, R>, grid, dim3(static_cast<unsigned>(cv)), 0,
+                          stream, static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
+                          static_cast<uint4 *>(y), rows, row_vecs, cv);
+        }
+        // Narrower rows: one resident wave of grid-stride CTAs.  16-bit data
+        // takes fewer chunks per pass, the next pass's loads issued before
+        // this pass computes (eight elements a chunk make the compute long
+        // enough to hide behind them); fp32 more chunks, no prefetch.
         constexpr int T = WGS_GELU_THREADS, U = PF ? WGS_GELU_U16 : WGS_GELU_U;
         const int64_t n_vec = n / kVec;
         const int64_t need = ceil_div(n_vec, static_cast<int64_t>(T) * U);
