@@ -351,10 +351,14 @@ def test_gelu_f16_full_size():
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
 @pytest.mark.parametrize("rows,width", [(1, 1), (3, 7), (5, 3), (17, 768), (1025, 1536),
                                         (33, 1000), (2, 4100), (1, 768), (7, 1536),
-                                        (4097, 512), (3, 2048), (100, 256), (70000, 1024)])
+                                        (4097, 512), (3, 2048), (100, 256), (70000, 1024),
+                                        (50, 252), (9, 504), (2, 8192)])
 def test_gelu_widths_and_paths(rows, width, dtype):
-    """Grid-stride path, bulk-copy pipeline (rows of 64..256 16-byte chunks:
-    fewer rows than CTAs, one row, ragged last tiles) and the scalar path."""
+    """Every path of the forward: row-block CTAs for rows of at least 64
+    16-byte chunks (row counts not a multiple of the 4-row block, one row,
+    several column blocks above 256 chunks), the grid-stride kernel for
+    narrower rows (63 chunks: fp32 at width 252, 16-bit at 504) and the
+    scalar path for widths that are not whole chunks."""
     x, b = synth.gelu_input(rows, width, dtype, seed=rows + width)
     y = wgs.bias_gelu_tanh(x.to(DEV), b.to(DEV))
     o, y64 = oracle.bias_gelu_tanh(x.numpy(), b.numpy())
