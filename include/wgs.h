@@ -37,13 +37,14 @@
  *   - The kernels run only on compute capability 10.3 (sm_103a); on any
  *     other device the entry points return WGS_ERR_ARCH.
  *   - Calls are thread-safe; the shared state is the per-device index
- *     error word read by wgs_check_error() (and the scratch array of
- *     bias_gelu_tanh_bwd_noalloc).
- *   - The first call of an entry point on a device (per dtype) caches what it needs
- *     from the runtime (SM count, resident CTAs per SM, symbol addresses),
- *     and so does window_bias_mask_add's first call with a new n; make those
- *     calls outside stream capture.  Other calls, captured or not, make no
- *     such query.
+ *     error words read by wgs_check_error() (and the scratch array of
+ *     bias_gelu_tanh_bwd_noalloc).  Kernels name the error words
+ *     directly, so no device address is kept between calls.
+ *   - The first call of an entry point on a device (per dtype) caches what it
+ *     needs from the runtime (SM count, resident CTAs per SM), and so does
+ *     window_bias_mask_add's first call with a new n; make those calls
+ *     outside stream capture.  Other calls, captured or not, make no such
+ *     query.  Both depend on the device only, not on its context.
  */
 #ifndef WGS_H
 #define WGS_H
@@ -282,9 +283,11 @@ wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bia
  *   `workspace`.  Sizes whose partial sums would not fit (more than
  *   1,048,576 floats: min(512, ceil(rows / 108)) slabs x width, so any row
  *   count up to width 2048) return WGS_ERR_TOO_LARGE and launch nothing.
- *   Allocates nothing.  The first call on a device looks up the array's
- *   device address (cudaGetSymbolAddress, with that device current); make
- *   that first call before any stream capture.
+ *   Allocates nothing.  Every call looks up the array's device address in
+ *   the calling thread's current context (cudaGetSymbolAddress, a host-side
+ *   lookup), so a device reset or a second context on the device is safe.
+ *   The first call in a context also loads the library's device code there:
+ *   make that first call before any stream capture.
  *   All calls on a device share the array, which keeps whatever the last
  *   call left there; nothing in it needs to start at zero, because every
  *   partial sum is written before it is read.  Calls whose work overlaps on
@@ -348,7 +351,10 @@ wgs_status window_bias_mask_add(const void *scores, const void *bias, const int3
  * Host memory only; no CUDA call is made. */
 
 /* Number of destination rows (product of the padded extents), or -1 for
- * invalid extents (grid or window < 1, padded < grid). */
+ * invalid extents: grid or window < 1, padded < grid, a rounded-up extent
+ * above INT32_MAX, or a product (of the padded extents or of the grid)
+ * that does not fit in int64.  The builders below return WGS_ERR_SHAPE for
+ * the same extents. */
 int64_t wgs_window_index_count(const int32_t grid[3], const int32_t window[3],
                                const int32_t *padded);
 
@@ -383,12 +389,13 @@ wgs_status wgs_build_shift_regions(const int32_t grid[3], const int32_t window[3
                                    const int32_t shift[3], const int32_t *padded, int32_t flags,
                                    int32_t axes_mask, int32_t *out_host, int64_t out_len);
 
-/* Read and clear the current device's index error word after the work
+/* Read and clear the current device's index error words after the work
  * already queued on `stream` has finished.  This call synchronises
  * `stream`.  Returns WGS_ERR_INDEX if any gather since the last check met
- * an index outside [-1, n_src), or any window_bias_mask_add a window type
- * outside [0, n_types); WGS_OK otherwise.  The word is shared by
- * every stream of the device. */
+ * an index outside [-1, n_src), any window reverse an inverse index outside
+ * [0, n_windowed), or any window_bias_mask_add a window type outside
+ * [0, n_types); WGS_OK otherwise.  The words are shared by every stream of
+ * the device. */
 wgs_status wgs_check_error(cudaStream_t stream);
 
 #ifdef __cplusplus

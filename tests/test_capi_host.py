@@ -103,6 +103,33 @@ def test_index_builder_errors(lib):
     assert lib.wgs_build_window_index(g, w, s, None, 0, out, 576) == OK
 
 
+def test_index_builders_reject_extents_whose_cell_count_overflows(lib):
+    """Padded extents near INT32_MAX multiply past INT64_MAX: the count is
+    -1 and every builder refuses with WGS_ERR_SHAPE before writing, even
+    with an out_len a wrapped product would have passed."""
+    big = 2 ** 31 - 1
+    g = (ctypes.c_int32 * 3)(2, 12, 24)
+    w = (ctypes.c_int32 * 3)(2, 6, 12)
+    s = (ctypes.c_int32 * 3)(1, 3, 6)
+    huge = (ctypes.c_int32 * 3)(big, big, big)
+    wide_grid = (ctypes.c_int32 * 3)(big, big, 4)     # grid cells overflow too
+    one = (ctypes.c_int32 * 3)(1, 1, 1)
+    out = (ctypes.c_int32 * 8)(*([7] * 8))
+    assert lib.wgs_window_index_count(g, w, huge) == -1
+    assert lib.wgs_window_index_count(wide_grid, one, None) == -1
+    # rounding a grid extent up to whole windows may not pass INT32_MAX
+    assert lib.wgs_window_index_count((ctypes.c_int32 * 3)(1, 1, big), (ctypes.c_int32 * 3)(1, 1, 2),
+                                      None) == -1
+    for fn in (lib.wgs_build_window_index, lib.wgs_build_window_inverse):
+        assert fn(g, w, s, huge, 0, out, 2 ** 62) == SHAPE
+        assert fn(wide_grid, one, s, None, 0, out, 2 ** 62) == SHAPE
+    assert lib.wgs_build_shift_regions(g, w, s, huge, 0, 7, out, 2 ** 62) == SHAPE
+    assert list(out) == [7] * 8  # nothing written
+    # the largest padded volume that fits still counts exactly
+    fits = (ctypes.c_int32 * 3)(2, 2 ** 30, 2 ** 30)
+    assert lib.wgs_window_index_count(g, w, fits) == 2 ** 61
+
+
 # ------------------------------------------------ argument checking ----
 
 def test_ln_argument_errors(lib):

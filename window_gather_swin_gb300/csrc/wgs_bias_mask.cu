@@ -25,6 +25,9 @@
 
 #include "wgs_common.cuh"
 
+#ifndef WGS_BM_EARLY
+#define WGS_BM_EARLY 1  // L2 prefetch of the first unit's logits before the wait
+#endif
 #ifndef WGS_BM_U
 #define WGS_BM_U 2  // rows in flight per thread
 #endif
@@ -36,6 +39,30 @@
 #endif
 
 namespace wgs {
+
+namespace {
+
+// Set (never cleared by a kernel) when a window type lies outside
+// [0, n_types); read and cleared by wgs_check_error through
+// bias_mask_error_take.  Kernels name it directly, so no device address is
+// kept on the host.
+__device__ unsigned int g_mask_error;
+
+}  // namespace
+
+// Enqueue on `stream` a copy of the bias-mask error word into *seen and a
+// reset of the word to zero; the caller synchronises the stream.
+wgs_status bias_mask_error_take(unsigned int *seen, cudaStream_t stream) {
+    static const unsigned int cleared = 0;
+    if (cudaMemcpyFromSymbolAsync(seen, g_mask_error, sizeof(*seen), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_mask_error, &cleared, sizeof(cleared), 0,
+                                cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+        cudaGetLastError();  // clear this thread's error
+        return WGS_ERR_CUDA;
+    }
+    return WGS_OK;
+}
 
 namespace {
 
@@ -77,11 +104,26 @@ __device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t
 template <typename E, int U>
 __global__ void __launch_bounds__(kMaxChunksPerRow > WGS_BM_THREADS ? kMaxChunksPerRow : WGS_BM_THREADS)
 bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
-                const int32_t *region, uint4 *out, unsigned int *err, uint32_t units, int32_t n,
+                const int32_t *region, uint4 *out, uint32_t units, int32_t n,
                 int32_t heads, int32_t n_types, int32_t cpr, int32_t rp, int32_t part_rows,
                 int32_t parts, FastDiv by_parts, FastDiv by_heads, uint32_t mask2) {
-    pdl_prologue();
     const int jc = static_cast<int>(threadIdx.x) % cpr, lr = static_cast<int>(threadIdx.x) / cpr;
+#if WGS_BM_EARLY
+    // L2 prefetch of the first unit's logits before waiting for the previous
+    // grid (a latency hint only: the loads come after the wait)
+    if (lr < rp && blockIdx.x < units) {
+        const uint32_t tile = div_by(blockIdx.x, by_parts);
+        const int32_t part = static_cast<int32_t>(blockIdx.x - tile * static_cast<uint32_t>(parts));
+        const int32_t i1 = (part + 1) * part_rows < n ? (part + 1) * part_rows : n;
+        const uint4 *sp = scores + static_cast<int64_t>(tile) * n * cpr + jc;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int32_t ii = part * part_rows + lr + u * rp;
+            if (ii < i1) prefetch_l2(sp + static_cast<int64_t>(ii) * cpr);
+        }
+    }
+#endif
+    pdl_prologue();
     if (lr >= rp) return;
     for (uint32_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const uint32_t tile = div_by(unit, by_parts);
@@ -128,7 +170,7 @@ bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
                         set_word(o, k, t);
                     }
                 } else {
-                    atomicOr(err, 1u);
+                    atomicOr(&g_mask_error, 1u);
                 }
                 st_stream(op + static_cast<int64_t>(ii) * cpr, o);
             }
@@ -140,7 +182,7 @@ bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
 template <typename E>
 __global__ void __launch_bounds__(256)
 bias_mask_scalar(const uint16_t *scores, const uint16_t *bias, const int32_t *win_type,
-                 const int32_t *region, uint16_t *out, unsigned int *err, int64_t total, int32_t n,
+                 const int32_t *region, uint16_t *out, int64_t total, int32_t n,
                  int32_t heads, int32_t n_types, uint32_t mask2) {
     pdl_prologue();
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -158,7 +200,7 @@ bias_mask_scalar(const uint16_t *scores, const uint16_t *bias, const int32_t *wi
             }
             o = static_cast<uint16_t>(t);
         } else {
-            atomicOr(err, 1u);
+            atomicOr(&g_mask_error, 1u);
         }
         out[e] = o;
     }
@@ -166,7 +208,7 @@ bias_mask_scalar(const uint16_t *scores, const uint16_t *bias, const int32_t *wi
 
 template <typename E>
 wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t *win_type,
-                            const int32_t *region, void *out, unsigned int *err, int64_t n_win,
+                            const int32_t *region, void *out, int64_t n_win,
                             int32_t heads, int32_t n, int32_t n_types, uint32_t mask2,
                             const DeviceInfo &dev, cudaStream_t stream) {
     const int64_t rows = n_win * heads * n;
@@ -202,7 +244,7 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
         return launch(kernel, dim3(static_cast<unsigned>(units < cap ? units : cap)),
                       dim3(static_cast<unsigned>(rp * cpr)), 0, stream,
                       static_cast<const uint4 *>(scores), static_cast<const uint4 *>(bias),
-                      win_type, region, static_cast<uint4 *>(out), err,
+                      win_type, region, static_cast<uint4 *>(out),
                       static_cast<uint32_t>(units), n, heads, n_types, cpr, rp, part_rows, parts,
                       make_fastdiv(static_cast<uint32_t>(parts)),
                       make_fastdiv(static_cast<uint32_t>(heads)), mask2);
@@ -213,7 +255,7 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
     return launch(bias_mask_scalar<E>, dim3(static_cast<unsigned>(need < cap ? need : cap)),
                   dim3(256), 0, stream, static_cast<const uint16_t *>(scores),
                   static_cast<const uint16_t *>(bias), win_type, region,
-                  static_cast<uint16_t *>(out), err, total, n, heads, n_types, mask2);
+                  static_cast<uint16_t *>(out), total, n, heads, n_types, mask2);
 }
 
 }  // namespace
@@ -248,9 +290,6 @@ extern "C" wgs_status window_bias_mask_add(const void *scores, const void *bias,
     DeviceInfo dev;
     wgs_status st = current_device(&dev);
     if (st != WGS_OK) return st;
-    unsigned int *err = nullptr;
-    st = index_error_word(dev.device, &err);
-    if (st != WGS_OK) return st;
     // the mask value rounded once to the tensor's format, in both halves
     uint16_t m16;
     if (dtype == WGS_F16) {
@@ -262,8 +301,8 @@ extern "C" wgs_status window_bias_mask_add(const void *scores, const void *bias,
     }
     const uint32_t mask2 = static_cast<uint32_t>(m16) | (static_cast<uint32_t>(m16) << 16);
     if (dtype == WGS_F16)
-        return launch_bias_mask<Fp16>(scores, bias, win_type, region, out, err, n_win, heads, n,
+        return launch_bias_mask<Fp16>(scores, bias, win_type, region, out, n_win, heads, n,
                                       n_types, mask2, dev, stream);
-    return launch_bias_mask<Bf16>(scores, bias, win_type, region, out, err, n_win, heads, n,
+    return launch_bias_mask<Bf16>(scores, bias, win_type, region, out, n_win, heads, n,
                                   n_types, mask2, dev, stream);
 }

@@ -28,10 +28,9 @@ struct DeviceInfo {
 };
 wgs_status current_device(DeviceInfo *info);
 
-// Device address of the index error word (read by wgs_check_error) on
-// `device`, which must be current; for kernels of other translation units.
-// Looked up on the first call per device.
-wgs_status index_error_word(int device, unsigned int **out);
+// Enqueue on `stream` a copy of the bias-mask add's error word into *seen
+// and its reset to zero (for wgs_check_error; the caller synchronises).
+wgs_status bias_mask_error_take(unsigned int *seen, cudaStream_t stream);
 
 // Launch `kernel` on `stream`.  With WGS_PDL the launch allows programmatic
 // dependent launch: the grid may be scheduled while the previous kernel on
@@ -88,6 +87,20 @@ __device__ __forceinline__ void pdl_prologue() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
 }
+
+// Ask L2 to fetch the 128-byte line holding p.  No data reaches the
+// thread, so a prefetch issued before griddepcontrol.wait cannot feed a
+// result with a stale value: L2 is the coherence point for every SM, and a
+// line that the previous grid writes afterwards is updated in L2.  Only a
+// latency hint; p must lie inside a live allocation.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 4-byte global load cached in L2 only (never in the SM's L1), so a value
+// read before griddepcontrol.wait leaves no stale copy in L1 for a later
+// load of the same address.
+__device__ __forceinline__ int32_t ld_cg_i32(const int32_t *p) { return __ldcg(p); }
 
 // 16-byte global load that skips L1 (each byte is read exactly once).
 __device__ __forceinline__ uint4 ld_stream(const void *p) {

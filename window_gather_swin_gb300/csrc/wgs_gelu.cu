@@ -31,6 +31,9 @@
 
 #include "wgs_common.cuh"
 
+#ifndef WGS_GELU_EARLY
+#define WGS_GELU_EARLY 1  // row-block form: L2 prefetch of the first chunks before the wait
+#endif
 #ifndef WGS_GELU_THREADS
 #define WGS_GELU_THREADS 256
 #endif
@@ -235,10 +238,20 @@ template <typename E, int R>
 __global__ void __launch_bounds__(256)
 bias_gelu_rows_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
                       int32_t row_vecs, int32_t cv) {
-    pdl_prologue();
     const int32_t c = static_cast<int32_t>(blockIdx.y) * cv + static_cast<int32_t>(threadIdx.x);
-    if (c >= row_vecs) return;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
+#if WGS_GELU_EARLY
+    // L2 prefetch of this thread's chunks before waiting for the previous
+    // grid (a latency hint only: the loads below come after the wait)
+    if (c < row_vecs) {
+        prefetch_l2(bias + c);
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (r0 + q < rows) prefetch_l2(x + (r0 + q) * row_vecs + c);
+    }
+#endif
+    pdl_prologue();
+    if (c >= row_vecs) return;
     const uint4 bv = __ldg(bias + c);
     uint4 xv[R];
 #pragma unroll

@@ -29,12 +29,13 @@
 // format, so results do not depend on the device.  Both passes stream:
 // grad_y and x are read once and grad_x is written once; the partials are a
 // few MB at most.
-#include <atomic>
-#include <mutex>
 #include <type_traits>
 
 #include "wgs_common.cuh"
 
+#ifndef WGS_BWD_EARLY
+#define WGS_BWD_EARLY 1  // pass 1: L2 prefetch of the first step before the wait
+#endif
 #ifndef WGS_BWD_ROWS
 #define WGS_BWD_ROWS 2  // rows per step per thread (two steps in flight)
 #endif
@@ -205,7 +206,6 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, float *partial,
                 int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb, int32_t groups,
                 int32_t slabs) {
-    pdl_prologue();
     constexpr bool k16 = !std::is_same<E, F32>::value;
     constexpr int kN = k16 ? 8 : 4;
     extern __shared__ float red[];  // [groups][cvb][kN]
@@ -213,6 +213,22 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     const int32_t cv = static_cast<int32_t>(blockIdx.y) * cvb + j;
     const bool active = g < groups && cv < row_chunks;
     const int64_t r0 = rows * blockIdx.x / slabs, r1 = rows * (blockIdx.x + 1) / slabs;
+#if WGS_BWD_EARLY
+    // L2 prefetch of the first step's chunks before waiting for the
+    // previous grid (a latency hint only: the loads come after the wait)
+    if (active) {
+        prefetch_l2(bias + cv);
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t r = r0 + g + static_cast<int64_t>(q) * groups;
+            if (r < r1) {
+                prefetch_l2(gy + r * row_chunks + cv);
+                prefetch_l2(x + r * row_chunks + cv);
+            }
+        }
+    }
+#endif
+    pdl_prologue();
     float2 acc[kN / 2];
 #pragma unroll
     for (int e = 0; e < kN / 2; ++e) acc[e] = make_float2(0.f, 0.f);
@@ -485,22 +501,20 @@ constexpr size_t kNoAllocScratchFloats = size_t{1} << 20;  // 4 MiB per device
 static __device__ __align__(256) float g_bwd_scratch[kNoAllocScratchFloats];
 
 // Host code cannot use g_bwd_scratch as a pointer (on the host it names a
-// stand-in object, not device memory), so each device's address is looked
-// up once, with that device current, and kept here.
-std::mutex g_scratch_mutex;
-float *g_scratch_ptr[64] = {};
-
-wgs_status scratch_for(int device, float **out) {
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[device]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();  // clear this thread's error
-            return WGS_ERR_CUDA;
-        }
-        g_scratch_ptr[device] = static_cast<float *>(p);
+// stand-in object, not device memory), so its device address is looked up
+// with cudaGetSymbolAddress, in the context current on the calling thread.
+// The lookup runs on every call: it is a host-side table lookup that
+// allocates nothing, and an address kept from an earlier call could name
+// memory of a context that no longer exists (after cudaDeviceReset) or is
+// not current (another context on the same device).  The first lookup in a
+// context also loads this library's device code there.
+wgs_status scratch_address(float **out) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();  // clear this thread's error
+        return WGS_ERR_CUDA;
     }
-    *out = g_scratch_ptr[device];
+    *out = static_cast<float *>(p);
     return WGS_OK;
 }
 
@@ -518,7 +532,7 @@ extern "C" wgs_status bias_gelu_tanh_bwd_noalloc(const void *grad_y, const void 
     const wgs_status ds = current_device(&dev);
     if (ds != WGS_OK) return ds;
     float *scratch = nullptr;
-    const wgs_status ss = scratch_for(dev.device, &scratch);
+    const wgs_status ss = scratch_address(&scratch);
     if (ss != WGS_OK) return ss;
     // Pass 1 writes every partial sum that pass 2 reads, in stream order, so
     // nothing in the array needs clearing between calls.

@@ -19,13 +19,28 @@ int64_t wrap(int64_t a, int64_t m) {
     return r < 0 ? r + m : r;
 }
 
+// a * b for positive a, b, or false when the product passes INT64_MAX.
+bool mul_fits(int64_t a, int64_t b, int64_t *out) {
+    if (a > INT64_MAX / b) return false;
+    *out = a * b;
+    return true;
+}
+
+// Padded extents (given, or the grid rounded up to whole windows), the cell
+// count of the padded grid and of the grid.  False for a non-positive grid
+// or window, a padded extent below the grid or above INT32_MAX, or a cell
+// count past INT64_MAX.
 bool padded_extents(const int32_t grid[3], const int32_t window[3], const int32_t *padded,
-                    int64_t ext[3]) {
+                    int64_t ext[3], int64_t *cells, int64_t *grid_cells) {
+    int64_t n = 1, g = 1;
     for (int k = 0; k < 3; ++k) {
         if (grid[k] < 1 || window[k] < 1) return false;
         ext[k] = padded ? padded[k] : ceil_div(grid[k], window[k]) * window[k];
-        if (ext[k] < grid[k]) return false;
+        if (ext[k] < grid[k] || ext[k] > INT32_MAX) return false;
+        if (!mul_fits(n, ext[k], &n) || !mul_fits(g, grid[k], &g)) return false;
     }
+    *cells = n;
+    *grid_cells = g;
     return true;
 }
 
@@ -34,9 +49,9 @@ bool padded_extents(const int32_t grid[3], const int32_t window[3], const int32_
 extern "C" int64_t wgs_window_index_count(const int32_t grid[3], const int32_t window[3],
                                           const int32_t *padded) {
     if (!grid || !window) return -1;
-    int64_t ext[3];
-    if (!padded_extents(grid, window, padded, ext)) return -1;
-    return ext[0] * ext[1] * ext[2];
+    int64_t ext[3], cells, grid_cells;
+    if (!padded_extents(grid, window, padded, ext, &cells, &grid_cells)) return -1;
+    return cells;
 }
 
 extern "C" wgs_status wgs_build_window_index(const int32_t grid[3], const int32_t window[3],
@@ -44,11 +59,11 @@ extern "C" wgs_status wgs_build_window_index(const int32_t grid[3], const int32_
                                              int32_t flags, int32_t *out_host, int64_t out_len) {
     if (!grid || !window || !shift || !out_host) return WGS_ERR_NULL;
     if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
-    int64_t ext[3];
-    if (!padded_extents(grid, window, padded, ext)) return WGS_ERR_SHAPE;
+    int64_t ext[3], cells, grid_cells;
+    if (!padded_extents(grid, window, padded, ext, &cells, &grid_cells)) return WGS_ERR_SHAPE;
     const int64_t G[3] = {grid[0], grid[1], grid[2]};
-    if (G[0] * G[1] * G[2] > INT32_MAX) return WGS_ERR_SHAPE;
-    if (out_len < ext[0] * ext[1] * ext[2]) return WGS_ERR_SHAPE;
+    if (grid_cells > INT32_MAX) return WGS_ERR_SHAPE;  // source tokens are INT32
+    if (out_len < cells) return WGS_ERR_SHAPE;
 
     // The roll is taken modulo the grid (shift then pad) or the padded grid
     // (pad then shift).
@@ -96,11 +111,11 @@ extern "C" wgs_status wgs_build_window_inverse(const int32_t grid[3], const int3
                                                int32_t flags, int32_t *inv_host, int64_t out_len) {
     if (!grid || !window || !shift || !inv_host) return WGS_ERR_NULL;
     if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
-    int64_t P[3];
-    if (!padded_extents(grid, window, padded, P)) return WGS_ERR_SHAPE;
+    int64_t P[3], cells, grid_cells;
+    if (!padded_extents(grid, window, padded, P, &cells, &grid_cells)) return WGS_ERR_SHAPE;
     const int64_t G[3] = {grid[0], grid[1], grid[2]};
-    if (P[0] * P[1] * P[2] > INT32_MAX) return WGS_ERR_SHAPE;
-    if (out_len < G[0] * G[1] * G[2]) return WGS_ERR_SHAPE;
+    if (cells > INT32_MAX) return WGS_ERR_SHAPE;  // windowed rows are INT32
+    if (out_len < grid_cells) return WGS_ERR_SHAPE;
     const bool roll_padded = flags == WGS_PAD_THEN_SHIFT;
     int64_t period[3], s[3], w[3];
     for (int k = 0; k < 3; ++k) {
@@ -138,9 +153,9 @@ extern "C" wgs_status wgs_build_shift_regions(const int32_t grid[3], const int32
     if (!grid || !window || !shift || !out_host) return WGS_ERR_NULL;
     if (flags != WGS_SHIFT_THEN_PAD && flags != WGS_PAD_THEN_SHIFT) return WGS_ERR_SHAPE;
     if (axes_mask < 0 || axes_mask > 7) return WGS_ERR_SHAPE;
-    int64_t ext[3];
-    if (!padded_extents(grid, window, padded, ext)) return WGS_ERR_SHAPE;
-    if (out_len < ext[0] * ext[1] * ext[2]) return WGS_ERR_SHAPE;
+    int64_t ext[3], cells, grid_cells;
+    if (!padded_extents(grid, window, padded, ext, &cells, &grid_cells)) return WGS_ERR_SHAPE;
+    if (out_len < cells) return WGS_ERR_SHAPE;
     // seam[k]: first cell past the seam along k (ext[k] when the axis is
     // not masked or not moved, so no cell is past it)
     int64_t seam[3];
