@@ -12,9 +12,13 @@ Window (2,6,12), shift (1,3,6).  Inputs are seeded synthetic tensors.
 Metric: effective HBM GB/s (algorithmic bytes: each input read once, each
 output written once, plus the index array) and ms per call per kernel.
 Beyond the step the line carries the other rows of the path (block-boundary
-fusions, bfloat16 forms, the GELU backward, the attention bias-mask add),
-a GELU rows sweep (1k-256k rows), the end-to-end figure from pinned host
-memory, and the oracle's single-thread CPU rate.
+fusions, the C=384 gathers over whole windows, bfloat16 forms, the GELU
+backward, the attention bias-mask add), a GELU rows sweep (1k-256k rows),
+the end-to-end figure from pinned host memory, the oracle's rate on the
+host CPU (one thread on a quarter of the rows, and all cores on every row),
+and, as its last two keys, the LayerNorm-family kernels' figures
+(headline_kernels) and the parity gate: every output element the timed
+buffers hold, read back after timing and compared with the oracle's.
 A step's ten launches are captured once, through the public API, in a CUDA
 graph; the graph is replayed K times back to back and CUDA events on the
 launching stream bracket the K replays.  One step touches 1.77 GB (13x the
@@ -38,10 +42,12 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from window_gather_swin_gb300 import synth  # noqa: E402
@@ -58,19 +64,37 @@ CPU_SAMPLE_FRACTION = 0.25
 class Call:
     """One kernel invocation of the step with its inputs, outputs and bytes."""
 
-    def __init__(self, name, workload, nbytes, inputs, outputs, run, oracle_run, rows):
+    def __init__(self, name, workload, nbytes, inputs, outputs, run, oracle, rows):
         self.name = name
         self.workload = workload
         self.bytes = int(nbytes)
         self.inputs = inputs        # {key: cpu tensor}
         self.outputs = outputs      # {key: (shape, dtype)}
         self.run = run              # run(dev_inputs, dev_outputs)
-        self.oracle_run = oracle_run  # oracle_run(fraction) -> (seconds, algorithmic bytes)
+        self.oracle = oracle        # OracleLeg of the call, or None
         self.rows = rows
 
     @property
     def label(self):
         return f"{self.name} {self.workload}"
+
+
+class OracleLeg:
+    """The oracle's side of one call, over a range [lo, hi) of its `units`
+    (token rows, or destination rows for the gathers):
+      compute(lo, hi) -> the oracle's outputs for those units (what is timed);
+      nbytes(lo, hi)  -> their algorithmic bytes;
+      check(gpu, orc, lo, hi) -> statistics of the GPU outputs of the same
+          units against the oracle's under the parity rules of
+          tests/parity.py; raises AssertionError on a violation.
+    The oracle legs build their window maps with the oracle's own builder,
+    so nothing here calls into the CUDA library."""
+
+    def __init__(self, units, compute, nbytes, check):
+        self.units = units
+        self.compute = compute
+        self.nbytes = nbytes
+        self.check = check
 
 
 # The workload both arms report: the ten launches of one step.
@@ -82,7 +106,94 @@ STEP_CONFIG = {
 }
 
 
-def build_calls():
+def _orc():
+    # The oracle is test infrastructure; only the CPU legs of this benchmark
+    # (cpu_baseline, the parity gate and the reference arm) execute it.
+    import oracle
+    return oracle
+
+
+def _rules():
+    # the comparison rules of the GPU parity tests, for the parity gate
+    from tests import parity
+    return parity
+
+
+def _oracle_map(st):
+    return _orc().build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+
+
+def _ln_leg(x, n, c):
+    x = x.numpy()
+
+    def check(g, o, lo, hi):
+        return {"ln": _rules().check_ln(g["y"], o["y"], _orc().ln_f64(x[lo:hi], EPS), "ln_fwd")}
+    return OracleLeg(n, lambda lo, hi: {"y": _orc().ln(x[lo:hi], EPS)},
+                     lambda lo, hi: 4 * (hi - lo) * c, check)
+
+
+def _add_ln_leg(a, b, n, c):
+    a, b = a.numpy(), b.numpy()
+
+    def compute(lo, hi):
+        r, y = _orc().residual_add_ln(a[lo:hi], b[lo:hi], EPS)
+        return {"r": r, "y": y}
+
+    def check(g, o, lo, hi):
+        _rules().assert_bitwise(g["r"], o["r"], "residual_out")
+        return {"bitwise": g["r"].size,
+                "ln": _rules().check_ln(g["y"], o["y"], _orc().ln_f64(o["r"], EPS), "add_ln y")}
+    return OracleLeg(n, compute, lambda lo, hi: 8 * (hi - lo) * c, check)
+
+
+def _gather_leg(src, st, norm):
+    src = src.numpy()
+    n, c = src.shape
+    idx = _oracle_map(st)
+    m = idx.size
+
+    def compute(lo, hi):
+        if norm:
+            dst, bad = _orc().norm_gather(src, idx[lo:hi], EPS)
+        else:
+            dst, bad = _orc().window_gather(src, idx[lo:hi])
+        return {"dst": dst, "bad": bad}
+
+    def check(g, o, lo, hi):
+        assert o["bad"] == 0, "the oracle's own map holds an index outside [-1, n_src)"
+        if not norm:
+            _rules().assert_bitwise(g["dst"], o["dst"], "window_gather")
+            return {"bitwise": g["dst"].size}
+        i = idx[lo:hi]
+        pad = i < 0
+        _rules().assert_bitwise(g["dst"][pad], o["dst"][pad], "norm_gather pad rows")
+        assert not o["dst"][pad].view(np.uint16).any(), "oracle pad rows are not zero"
+        ln = _rules().check_ln(g["dst"][~pad], o["dst"][~pad], _orc().ln_f64(src[i[~pad]], EPS),
+                               "norm_gather")
+        return {"bitwise": g["dst"][pad].size, "ln": ln}
+    return OracleLeg(m, compute, lambda lo, hi: (hi - lo) / m * (2 * c * n) + (hi - lo) * (2 * c + 4),
+                     check)
+
+
+def _gelu_leg(x, b, rows, width, esz):
+    x, b = x.numpy(), b.numpy()
+
+    def compute(lo, hi):
+        return {"y": _orc().bias_gelu_tanh(x[lo:hi], b, want_f64=False)[0]}
+
+    def check(g, o, lo, hi):
+        y, y64 = _orc().bias_gelu_tanh(x[lo:hi], b, want_f64=True)  # unrounded values
+        assert np.array_equal(y.view(np.uint8), o["y"].view(np.uint8)), "oracle not repeatable"
+        if esz == 4:
+            return {"gelu_f32": _rules().check_gelu_f32(g["y"], y64, "bias_gelu fp32")}
+        return {"gelu_f16": _rules().check_fp16_near(g["y"], y, y64, "bias_gelu fp16")}
+    return OracleLeg(rows, compute, lambda lo, hi: 2 * (hi - lo) * width * esz + width * esz, check)
+
+
+def build_calls(gpu=True):
+    """The ten calls of one step.  With gpu=False (the reference arm) the
+    index maps come from the oracle's builder and nothing touches the CUDA
+    library; the maps are identical either way."""
     import window_gather_swin_gb300 as wgs
     calls = []
     for st in (synth.STAGE_192, synth.STAGE_384):
@@ -90,35 +201,29 @@ def build_calls():
         x = synth.ln_input(n, c, seed=1)
         calls.append(Call(
             "ln_fwd", f"[{n},{c}]", 4 * n * c, {"x": x}, {"y": ((n, c), torch.float16)},
-            lambda i, o: wgs.ln_fwd(i["x"], EPS, out=o["y"]),
-            _oracle_rows(lambda f, x=x, n=n: _t(lambda: _orc().ln(x[: _k(n, f)].numpy(), EPS)),
-                         lambda f, n=n, c=c: 4 * _k(n, f) * c), n))
+            lambda i, o: wgs.ln_fwd(i["x"], EPS, out=o["y"]), _ln_leg(x, n, c), n))
         a, b = synth.residual_branch(n, c, seed=2)
         calls.append(Call(
             "residual_add_ln_fwd", f"[{n},{c}]", 8 * n * c, {"a": a, "b": b},
             {"r": ((n, c), torch.float16), "y": ((n, c), torch.float16)},
             lambda i, o: wgs.residual_add_ln_fwd(i["a"], i["b"], EPS, residual_out=o["r"], out=o["y"]),
-            _oracle_rows(lambda f, a=a, b=b, n=n: _t(lambda: _orc().residual_add_ln(
-                a[: _k(n, f)].numpy(), b[: _k(n, f)].numpy(), EPS)),
-                lambda f, n=n, c=c: 8 * _k(n, f) * c), n))
+            _add_ln_leg(a, b, n, c), n))
         src = synth.gather_source(n, c, seed=3)
-        idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+        if gpu:
+            idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, st.padded)
+        else:
+            idx = torch.from_numpy(_oracle_map(st))
         m = idx.numel()
         gbytes = 2 * c * n + 2 * c * m + 4 * m
-        for name, fn in (("window_gather", "g"), ("norm_gather", "n")):
-            if fn == "g":
+        for name in ("window_gather", "norm_gather"):
+            if name == "window_gather":
                 run = lambda i, o: wgs.window_gather(i["src"], i["idx"], out=o["dst"])
-                orc = lambda f, src=src, idx=idx, m=m: _t(lambda: _orc().window_gather(
-                    src.numpy(), idx[: _k(m, f)].numpy()))
             else:
                 run = lambda i, o: wgs.norm_gather(i["src"], i["idx"], EPS, out=o["dst"])
-                orc = lambda f, src=src, idx=idx, m=m: _t(lambda: _orc().norm_gather(
-                    src.numpy(), idx[: _k(m, f)].numpy(), EPS))
             calls.append(Call(
                 name, f"[{n},{c}]->{m}", gbytes, {"src": src, "idx": idx},
                 {"dst": ((m, c), torch.float16)}, run,
-                _oracle_rows(orc, lambda f, n=n, m=m, c=c: _k(m, f) / m * (2 * c * n) + _k(m, f) * (2 * c + 4)),
-                m))
+                _gather_leg(src, st, norm=name == "norm_gather"), m))
     for (rows, width), dt, seed in ((synth.GELU_F32_SHAPE, torch.float32, 4),
                                     (synth.GELU_F16_SHAPE, torch.float16, 4)):
         x, b = synth.gelu_input(rows, width, dt, seed=seed)
@@ -128,10 +233,7 @@ def build_calls():
             2 * rows * width * esz + width * esz, {"x": x, "bias": b},
             {"y": ((rows, width), dt)},
             lambda i, o: wgs.bias_gelu_tanh(i["x"], i["bias"], out=o["y"]),
-            _oracle_rows(lambda f, x=x, b=b, rows=rows: _t(lambda: _orc().bias_gelu_tanh(
-                x[: _k(rows, f)].numpy(), b.numpy(), want_f64=False)),
-                lambda f, rows=rows, width=width, esz=esz: 2 * _k(rows, f) * width * esz + width * esz),
-            rows))
+            _gelu_leg(x, b, rows, width, esz), rows))
     return calls
 
 
@@ -162,6 +264,19 @@ def build_next_calls():
             lambda i, o: wgs.residual_add_norm_gather(i["a"], i["b"], i["idx"], EPS,
                                                       residual_out=o["r"], out=o["dst"]),
             None, m))
+    # C = 384 with whole windows (4x96x96, 36864 rows): the map a block at
+    # that stage uses end to end, since its attention needs equal windows
+    st = synth.STAGE_384
+    n, c = st.tokens, st.width
+    idx = wgs.build_window_index(st.grid, synth.WINDOW, synth.SHIFT, synth.ATTN_384.padded)
+    m = idx.numel()
+    src = synth.gather_source(n, c, seed=3)
+    calls.append(Call("window_gather", f"[{n},{c}]->{m}", 2 * c * n + (2 * c + 4) * m,
+                      {"src": src, "idx": idx}, {"dst": ((m, c), torch.float16)},
+                      lambda i, o: wgs.window_gather(i["src"], i["idx"], out=o["dst"]), None, m))
+    calls.append(Call("norm_gather", f"[{n},{c}]->{m}", 2 * c * n + (2 * c + 4) * m,
+                      {"src": src, "idx": idx}, {"dst": ((m, c), torch.float16)},
+                      lambda i, o: wgs.norm_gather(i["src"], i["idx"], EPS, out=o["dst"]), None, m))
     # bfloat16 forms at the large stage / MLP width
     st = synth.STAGE_192
     n, c = st.tokens, st.width
@@ -231,27 +346,6 @@ def build_next_calls():
             lambda i, o: wgs.window_bias_mask_add(i["s"], i["b"], None, i["reg"], out=o["out"]),
             None, ast.n_win * ast.heads * ast.n))
     return calls
-
-
-def _k(n, f):
-    return max(1, int(n * f))
-
-
-def _t(fn):
-    t0 = time.perf_counter()
-    fn()
-    return time.perf_counter() - t0
-
-
-def _oracle_rows(timer, nbytes):
-    return lambda f: (timer(f), nbytes(f))
-
-
-def _orc():
-    # The oracle is test infrastructure; only the CPU-baseline and the
-    # reference arm of this benchmark execute it.
-    import oracle
-    return oracle
 
 
 # ---------------------------------------------------------------- util ----
@@ -407,17 +501,155 @@ def barrier(world):
 
 # ------------------------------------------------------------ our arm ----
 
-def cpu_baseline(calls):
-    """The oracle, as it stands, single-threaded, on the first quarter of the
-    rows of every call of one step."""
+def host_cpu():
+    """Cores this process may run on, and the host CPU's model name."""
+    cores = len(os.sched_getaffinity(0))
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return cores, model
+
+
+def _ranges(n, parts):
+    step = max(1, -(-n // parts))
+    return [(lo, min(n, lo + step)) for lo in range(0, n, step)]
+
+
+def oracle_step(calls, threads, fraction=1.0):
+    """The oracle, as it stands, on the first `fraction` of the units of
+    every call of `calls`.  With threads > 1 each call's units are split
+    into row ranges run on that many host threads (the oracle's C code runs
+    outside the GIL).  Returns (seconds, algorithmic bytes, outputs), where
+    outputs[j] lists ((lo, hi), oracle outputs) of call j; only the oracle
+    calls are timed."""
     secs = nbytes = 0.0
-    for c in calls:
-        s, b = c.oracle_run(CPU_SAMPLE_FRACTION)
-        secs += s
-        nbytes += b
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {CPU_SAMPLE_FRACTION:g} of the rows of each of the {len(calls)} calls of "
-                      f"one step ({nbytes / 1e6:.1f} MB algorithmic, {secs:.2f} s)"}
+    outs = []
+    ex = ThreadPoolExecutor(threads) if threads > 1 else None
+    try:
+        for c in calls:
+            leg = c.oracle
+            k = max(1, int(leg.units * fraction))
+            parts = _ranges(k, threads * 4) if ex else [(0, k)]
+            t0 = time.perf_counter()
+            res = list(ex.map(lambda r: leg.compute(*r), parts)) if ex else [leg.compute(0, k)]
+            secs += time.perf_counter() - t0
+            nbytes += leg.nbytes(0, k)
+            outs.append(list(zip(parts, res)))
+    finally:
+        if ex:
+            ex.shutdown()
+    return secs, nbytes, outs
+
+
+def cpu_legs(calls, gpu_outs, want_baseline, want_parity):
+    """The oracle on this host's CPU: Run 1 (one thread, the first quarter
+    of every call's units: the cpu_baseline value), Run 2 (every unit, split
+    over all usable cores, three repetitions, median) and the parity gate
+    (every output element the timed buffers hold against Run 2's outputs)."""
+    cores, model = host_cpu()
+    calls = [c for c in calls if c.oracle is not None]
+    base = parity = None
+    last = None
+    if want_baseline:
+        s1, b1, _ = oracle_step(calls, 1, CPU_SAMPLE_FRACTION)
+        reps = []
+        for _ in range(3):
+            s2, b2, last = oracle_step(calls, cores, 1.0)
+            reps.append(s2)
+        med = statistics.median(reps)
+        base = {"value": round(b1 / s1 / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": (f"first {CPU_SAMPLE_FRACTION:g} of the units of each of the {len(calls)} "
+                           f"calls of one step ({b1 / 1e6:.1f} MB algorithmic, {s1:.2f} s), one thread"),
+                "sample_fraction": CPU_SAMPLE_FRACTION,
+                "host_cores": cores, "cpu_model": model,
+                "run2_all_cores": {"value": round(b2 / med / 1e9, 4), "unit": "GB/s",
+                                   "cores": cores, "repetitions": len(reps),
+                                   "s_median": round(med, 3), "s_min": round(min(reps), 3),
+                                   "sample": "every unit of every call of one step"}}
+    if want_parity and gpu_outs is not None:
+        if last is None:
+            _, _, last = oracle_step(calls, cores, 1.0)
+        parity = parity_gate(calls, gpu_outs, last, cores)
+    return base, parity
+
+
+def parity_gate(calls, gpu_outs, orc_outs, threads):
+    """Element-by-element comparison of the GPU outputs of `calls` with the
+    oracle's, range by range, under the rules of tests/parity.py: identical
+    bits for residual_out, gathered and pad rows; LayerNorm outputs inside
+    the FP32 error bound and the 2e-3 bar (bar exceptions only as one-spacing
+    flips at a rounding midpoint); fp32 GELU within 1e-5 relative; fp16 GELU
+    inside the FP32 error bound."""
+    tot = {"bitwise": 0, "ln_n": 0, "ln_max_abs": 0.0, "ln_tie_flips": 0, "ln_err_over_bound": 0.0,
+           "gelu_f32_n": 0, "gelu_f32_max_rel": 0.0, "gelu_f16_n": 0, "gelu_f16_max_ulp": 0,
+           "gelu_f16_err_over_bound": 0.0}
+    failures = []
+
+    def one(j, lo, hi, o):
+        g = {k: v[lo:hi] for k, v in gpu_outs[j].items()}
+        return calls[j].oracle.check(g, o, lo, hi)
+
+    jobs = [(j, lo, hi, o) for j in range(len(calls)) for (lo, hi), o in orc_outs[j]]
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [(calls[j].label, ex.submit(one, j, lo, hi, o)) for j, lo, hi, o in jobs]
+        for label, f in futs:
+            try:
+                st = f.result()
+            except AssertionError as e:
+                failures.append(f"{label}: {str(e)[:300]}")
+                continue
+            tot["bitwise"] += int(st.get("bitwise", 0))
+            if "ln" in st:
+                ln = st["ln"]
+                tot["ln_n"] += ln["n"]
+                tot["ln_max_abs"] = max(tot["ln_max_abs"], ln["max_abs"])
+                tot["ln_tie_flips"] += ln.get("above_abs_tol_tie_flips", 0)
+                tot["ln_err_over_bound"] = max(tot["ln_err_over_bound"], ln["max_err_over_bound"])
+            if "gelu_f32" in st:
+                tot["gelu_f32_n"] += st["gelu_f32"]["n"]
+                tot["gelu_f32_max_rel"] = max(tot["gelu_f32_max_rel"], st["gelu_f32"]["max_rel"])
+            if "gelu_f16" in st:
+                gf = st["gelu_f16"]
+                tot["gelu_f16_n"] += gf["n"]
+                tot["gelu_f16_max_ulp"] = max(tot["gelu_f16_max_ulp"], gf["max_ulp"])
+                tot["gelu_f16_err_over_bound"] = max(tot["gelu_f16_err_over_bound"],
+                                                     gf["max_err_over_bound"])
+    elements = tot["bitwise"] + tot["ln_n"] + tot["gelu_f32_n"] + tot["gelu_f16_n"]
+    out = {"pass": not failures, "elements": elements, "bitwise": tot["bitwise"],
+           "ln": {"n": tot["ln_n"], "max_abs": tot["ln_max_abs"], "tie_flips": tot["ln_tie_flips"],
+                  "err_over_bound": round(tot["ln_err_over_bound"], 4)},
+           "gelu_f32": {"n": tot["gelu_f32_n"], "max_rel": tot["gelu_f32_max_rel"]},
+           "gelu_f16": {"n": tot["gelu_f16_n"], "max_ulp": tot["gelu_f16_max_ulp"],
+                        "err_over_bound": round(tot["gelu_f16_err_over_bound"], 4)},
+           "scope": (f"every output element of the {len(calls)} timed calls, read back from the "
+                     "timed buffers, against the oracle (rules of tests/parity.py)")}
+    if failures:
+        out["failures"] = failures[:5]
+    return out
+
+
+HEADLINE = ("ln_fwd", "residual_add_ln_fwd", "window_gather", "norm_gather")
+
+
+def headline_kernels(kernels):
+    """The LayerNorm-family step kernels at both stages, compactly: per
+    kernel [us per call, GB/s, fraction of the measured copy peak, fraction
+    of the nominal 8 TB/s]."""
+    out = {"fields": ["us_per_call", "GB/s", "of_measured_peak", "of_8TB/s"]}
+    for k in kernels:
+        if k["kernel"] in HEADLINE and not k["workload"].startswith("bf16"):
+            out[f"{k['kernel']} {k['workload']}"] = [round(k["ms_per_call"] * 1e3, 2), k["gbs"],
+                                                     k["frac_of_measured"], k["frac_of_nominal_8tbs"]]
+    return out
 
 
 def capture(fn, dev):
@@ -498,6 +730,11 @@ def run_ours(args, rank, world, local):
     wall = time.perf_counter() - t_wall
     barrier(world)
     clocks = sampler.stop()
+    # the outputs the timed replays left in buffer set 0, for the parity gate
+    gpu_outs = None
+    if rank == 0 and not args.no_parity:
+        gpu_outs = [{k: v.cpu().numpy() for k, v in o.items()} if c.oracle else None
+                    for c, o in zip(calls, sets[0][1])]
     region_ms = t0.elapsed_time(t1)
     max_region_ms = reduce_max(region_ms, world, dev)
     all_bytes = reduce_sum(step_bytes * K, world, dev)
@@ -550,16 +787,14 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "storage_dtype": "fp16 rows (LN, gathers, fp16 GELU), fp32 (fp32 GELU)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": {**(STEP_CONFIG if not args.only else {"workload": f"subset: {args.only}"}),
-                   "launches_per_step": len(calls),
-                   "l2": (f"inputs larger than L2: steps run back to back and one step touches "
-                          f"{step_bytes * n_sets / 1e6:.0f} MB over {n_sets} buffer set(s) "
-                          f"(L2 {l2 / 1e6:.0f} MB), so every input is read from HBM; no flush"),
-                   "timing": ("each step's launches are captured once in a CUDA graph through the "
-                              "public API and replayed K times; CUDA events around the K replays on "
-                              "the launching stream; value = all ranks' algorithmic bytes / slowest "
-                              "rank's region time"),
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(world, args.only, len(calls)),
+        "l2": (f"inputs larger than L2: steps run back to back and one step touches "
+               f"{step_bytes * n_sets / 1e6:.0f} MB over {n_sets} buffer set(s) "
+               f"(L2 {l2 / 1e6:.0f} MB), so every input is read from HBM; no flush"),
+        "timing": ("each step's launches are captured once in a CUDA graph through the "
+                   "public API and replayed K times; CUDA events around the K replays on "
+                   "the launching stream; value = all ranks' algorithmic bytes / slowest "
+                   "rank's region time"),
         "wall_s": round(wall, 3),
         "kernels": kernels,
         "kernels_in_step": in_step,
@@ -570,12 +805,29 @@ def run_ours(args, rank, world, local):
         "gpu_launches": K * len(calls),
         "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(calls)
+    parity = None
     if rank == 0:
+        base, parity = cpu_legs(calls, gpu_outs, world == 1 and not args.no_cpu_baseline,
+                                not args.no_parity)
+        if base:
+            line["cpu_baseline"] = base
+        # last, so that a reader of the line's tail sees them
+        line["headline_kernels"] = headline_kernels(kernels)
+        if parity:
+            line["parity"] = parity
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+    if parity and not parity["pass"]:
+        raise SystemExit("parity gate failed: " + "; ".join(parity.get("failures", [])))
+
+
+def step_config(world, only=None, launches=10, rank0_only=False):
+    """The `config` both arms print: the workload and how it is spread."""
+    cfg = dict(STEP_CONFIG) if not only else {"workload": f"subset: {only}"}
+    cfg["launches_per_step"] = launches
+    cfg["parallelism"] = f"rank 0 of {world}" if rank0_only and world > 1 else f"replicas x{world}"
+    return cfg
 
 
 def run_isolated(calls, dev, l2, peak, launches):
@@ -750,44 +1002,44 @@ def run_e2e(calls, dev, args, world):
 
 def run_reference(args, rank, world):
     """The oracle on the host cores, as the reference arm: each step runs
-    every call of the step on a bounded sample of its rows."""
+    every call of the step through the oracle, split over all usable cores,
+    on the largest leading fraction of its units that keeps the whole run
+    within --ref-budget-s (all of them for short runs).  Nothing here calls
+    into the CUDA library: the index maps come from the oracle's builder."""
     if world > 1:
         init_dist(world, "gloo")
         if rank != 0:
             torch.distributed.destroy_process_group()
             return
-    calls = build_calls()
-    # size the per-step sample so the whole run stays within ~2 minutes
-    probe = 1.0 / 1024
-    probe_s = sum(c.oracle_run(probe)[0] for c in calls)
+    calls = build_calls(gpu=False)
+    cores, model = host_cpu()
+    probe = 1.0 / 256
+    probe_s, _, _ = oracle_step(calls, cores, probe)
     full_step_s = probe_s / probe
-    budget_s = args.ref_budget_s
-    frac = budget_s / (full_step_s * (args.steps + args.warmup))
-    frac = max(1.0 / 16384, min(1.0 / 16, frac))
+    frac = args.ref_budget_s / (full_step_s * (args.steps + args.warmup))
+    frac = max(1.0 / 16384, min(1.0, frac))
     for _ in range(args.warmup):
-        for c in calls:
-            c.oracle_run(frac)
+        oracle_step(calls, cores, frac)
     secs = nbytes = 0.0
     for _ in range(args.steps):
-        for c in calls:
-            s, b = c.oracle_run(frac)
-            secs += s
-            nbytes += b
+        s_, b_, _ = oracle_step(calls, cores, frac)
+        secs += s_
+        nbytes += b_
     value = nbytes / secs / 1e9
-    sample = (f"first {frac:.3g} of the rows of each of the {len(calls)} calls per step "
-              f"({nbytes / args.steps / 1e6:.2f} MB algorithmic per step)")
+    sample = (f"first {frac:.3g} of the units of each of the {len(calls)} calls per step "
+              f"({nbytes / args.steps / 1e6:.2f} MB algorithmic per step), split over {cores} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": {**STEP_CONFIG, "launches_per_step": len(calls),
-                   "timing": ("each step runs the oracle on a row sample of every call of the step "
-                              "(see cpu_baseline.sample); time.perf_counter around each call"),
-                   "parallelism": "rank 0 only"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "config": step_config(world, None, len(calls), rank0_only=True),
+        "timing": ("each step runs the oracle on every call of the step (see cpu_baseline.sample); "
+                   "time.perf_counter around each call"),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample, "sample_fraction": frac, "host_cores": cores,
+                         "cpu_model": model},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -807,6 +1059,8 @@ def main(argv=None):
                    help="steps of the end-to-end leg from pinned host memory (at most --steps)")
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip timing the oracle on the host cores")
+    p.add_argument("--no-parity", action="store_true",
+                   help="skip the parity gate (the timed outputs against the oracle)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--ref-budget-s", type=float, default=120.0,
                    help="--impl reference: seconds of oracle work to aim for over the whole run")

@@ -348,6 +348,11 @@ wgs_status window_bias_mask_add(const void *scores, const void *bias, const int3
  *     -shift -- and every other cell is -1;
  *     WGS_PAD_THEN_SHIFT: the roll runs over the padded grid, and a rolled
  *     position outside the grid is -1.
+ * A block feeds one map to its gather, its attention (window_bias_mask_add)
+ * and its window reverse, and a batched attention needs equal windows: pass
+ * padded extents that are window multiples (padded == NULL does this), e.g.
+ * 4 x 96 x 96 for the 4 x 91 x 90 grid at window (2, 6, 12).  A map with a
+ * cut last window (4 x 96 x 90 there) is valid for the gathers alone.
  * Host memory only; no CUDA call is made. */
 
 /* Number of destination rows (product of the padded extents), or -1 for

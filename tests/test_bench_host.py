@@ -69,3 +69,68 @@ def test_reference_arm_under_two_ranks_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["config"]["workload"] == bench.STEP_CONFIG["workload"]
+
+
+def _stitch(outs):
+    """The oracle's range outputs of each call joined into whole arrays: a
+    stand-in for the GPU outputs read back from the timed buffers."""
+    import numpy as np
+    return [{k: np.concatenate([r[k] for _, r in o]) for k in o[0][1] if k != "bad"}
+            for o in outs]
+
+
+def test_parity_gate_passes_on_oracle_outputs_and_flags_planted_errors():
+    """The bench's parity gate on the first 1 % of every step call's rows:
+    the oracle's own outputs pass; one wrong bit in residual_out or a
+    gathered row, a normalised value off by 0.01, a nonzero pad row or an
+    fp32 GELU value off by 3e-5 relative each fail their call."""
+    import numpy as np
+    calls = bench.build_calls(gpu=False)
+    _, _, outs = bench.oracle_step(calls, 2, 0.01)
+    good = bench.parity_gate(calls, _stitch(outs), outs, 2)
+    assert good["pass"] and "failures" not in good
+    assert good["elements"] == sum(v.size for g in _stitch(outs) for v in g.values())
+    assert good["bitwise"] > 0 and good["ln"]["n"] > 0
+    assert good["gelu_f32"]["n"] > 0 and good["gelu_f16"]["n"] > 0
+    labels = [c.label for c in calls]
+    bad = _stitch(outs)
+    j = labels.index("residual_add_ln_fwd [131040,192]")
+    bad[j]["r"].view(np.uint16)[7, 3] ^= 1
+    j = labels.index("window_gather [32760,384]->34560")
+    bad[j]["dst"].view(np.uint16)[10, 5] ^= 0x8000
+    j = labels.index("norm_gather [131040,192]->138240")
+    row = int(np.nonzero(bench._oracle_map(bench.synth.STAGE_192)[:bad[j]["dst"].shape[0]] >= 0)[0][0])
+    bad[j]["dst"][row, 9] += np.float16(0.01)
+    j = labels.index("norm_gather [32760,384]->34560")
+    pads = np.nonzero(bench._oracle_map(bench.synth.STAGE_384)[:bad[j]["dst"].shape[0]] < 0)[0]
+    if pads.size:  # the first 1 % of the C = 384 map holds pad rows
+        bad[j]["dst"][pads[0], 0] = np.float16(1.0)
+    j = labels.index("bias_gelu_tanh fp32 [131040,768]")
+    bad[j]["y"][5, 5] *= np.float32(1 + 3e-5)
+    got = bench.parity_gate(calls, bad, outs, 2)
+    assert not got["pass"]
+    failed = {f.split(":")[0] for f in got["failures"]}
+    want = {"residual_add_ln_fwd [131040,192]", "window_gather [32760,384]->34560",
+            "norm_gather [131040,192]->138240", "bias_gelu_tanh fp32 [131040,768]"}
+    if pads.size:
+        want.add("norm_gather [32760,384]->34560")
+    assert failed == want
+
+
+def test_reference_arm_never_loads_the_cuda_library():
+    """The reference arm builds its index maps with the oracle, so a run of
+    it leaves libwgs.so unloaded."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys, json; sys.argv=['bench.py','--impl','reference','--steps','1','--warmup',"
+            "'1','--ref-budget-s','1']; import bench; bench.main(sys.argv[1:]); "
+            "maps=open('/proc/self/maps').read(); print(json.dumps({'wgs': 'libwgs.so' in maps}))")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert json.loads(lines[-1]) == {"wgs": False}
+    ref = json.loads(lines[0])
+    assert ref["impl"] == "reference" and ref["cpu_baseline"]["host_cores"] >= 1

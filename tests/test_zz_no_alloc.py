@@ -6,10 +6,11 @@ passes no allocator or workspace, or a hot path that must not call
 cudaMalloc because it can synchronise the device.  Its partial sums live in
 a fixed array inside the library instead of a workspace.  This file checks,
 through the C ABI, that it returns exactly what the workspace entry point
-returns, on two calls in a row with different inputs (the array keeps the
-previous call's contents, which must not leak into the next result), and
-that sizes beyond the array are refused.  It sits in its own file, named to
-be collected last.
+returns, on two calls in a row with different inputs and on a run of calls
+from the largest size the array takes down to smaller ones (the array
+keeps the previous call's contents, which must not leak into the next
+result), and that sizes beyond the array are refused.  It sits in its own
+file, named to be collected last.
 """
 import ctypes
 
@@ -55,6 +56,30 @@ def test_noalloc_backward_matches_the_workspace_entry_point_twice(dtype, rows, w
             # which is inside every tolerance the other tests apply
             assert torch.equal(gx.view(torch.uint8), want_gx.view(torch.uint8)), (call, "grad_x")
             assert torch.equal(gb.view(torch.uint8), want_gb.view(torch.uint8)), (call, "grad_bias")
+
+
+def test_noalloc_backward_larger_then_smaller_shapes_read_no_stale_partials():
+    """The first call fills the whole array (512 slabs x 2048 columns, the
+    largest size it takes); each later call has fewer slabs, a narrower row
+    or the scalar path, and new inputs.  A partial sum left by an earlier
+    call and read again would change grad_bias, so every result must equal
+    the workspace entry point's bit for bit."""
+    lib = _capi.load()
+    cases = [(torch.float16, 60000, 2048, 50), (torch.float16, 5000, 1024, 51),
+             (torch.float32, 777, 520, 52), (torch.bfloat16, 333, 13, 53)]
+    with torch.cuda.device(DEV):
+        for dtype, rows, width, seed in cases:
+            x, b = synth.gelu_input(rows, width, dtype, seed=seed)
+            gy, _ = synth.gelu_input(rows, width, dtype, seed=seed + 7)
+            x, b, gy = x.to(DEV), b.to(DEV), gy.to(DEV)
+            want_gx, want_gb = wgs.bias_gelu_tanh_bwd(gy, x, b)
+            gx = torch.full_like(x, float("nan"))
+            gb = torch.full_like(b, float("nan"))
+            assert _noalloc(lib, gy, x, b, gx, gb) == 0
+            torch.cuda.synchronize(DEV)
+            what = (str(dtype), rows, width)
+            assert torch.equal(gx.view(torch.uint8), want_gx.view(torch.uint8)), (what, "grad_x")
+            assert torch.equal(gb.view(torch.uint8), want_gb.view(torch.uint8)), (what, "grad_bias")
 
 
 def test_noalloc_backward_refuses_sizes_beyond_its_array():
