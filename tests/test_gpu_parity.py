@@ -672,7 +672,9 @@ def _spacing(v, fmt):
 def _check_bwd(gy, x, b, gx, gb, fmt, what):
     """grad_x against the oracle within the FP32 error bound; grad_bias
     against the exact sum of the GPU's own rounded grad_x within the bound
-    of a recursive FP32 sum (at most ~1024 additions deep)."""
+    of a recursive FP32 sum (at most ~1024 additions deep), and directly
+    against the oracle's grad_bias (the exact sum of its rounded grad_x)
+    within that bound plus the column's summed grad_x differences."""
     o_gx, o_gb, gx64, gb64 = oracle.bias_gelu_tanh_bwd(gy, x, b, fmt=fmt)
     gxv = _values(gx, fmt)
     gyv = _values(gy, fmt)
@@ -687,8 +689,15 @@ def _check_bwd(gy, x, b, gx, gb, fmt, what):
     gbv = _values(gb, fmt)
     lim = depth_bound + 0.5 * _spacing(gbv, fmt) + 1e-30
     assert np.all(np.abs(gbv - own) <= lim), (what, np.max(np.abs(gbv - own) / lim))
+    # |gb - gb64| <= |gb - own| + |own - gb64| and |own - gb64| is at most the
+    # column sum of |grad_x - oracle grad_x|
+    carried = np.abs(gxv - _values(o_gx, fmt)).sum(axis=0)
+    direct = lim + carried
+    assert np.all(np.abs(gbv - gb64) <= direct), (what, "grad_bias vs oracle",
+                                                  np.max(np.abs(gbv - gb64) / direct))
     return {"max_gx_err_over_bound": float((err[fin] / bound[fin]).max(initial=0)),
-            "max_gb_err_over_bound": float((np.abs(gbv - own) / lim).max(initial=0))}
+            "max_gb_err_over_bound": float((np.abs(gbv - own) / lim).max(initial=0)),
+            "max_gb_vs_oracle_over_bound": float((np.abs(gbv - gb64) / direct).max(initial=0))}
 
 
 def _bwd_inputs(rows, width, dtype, seed):

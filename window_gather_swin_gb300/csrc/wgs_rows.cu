@@ -21,6 +21,8 @@
 // U * CPL independent 16-byte loads in flight before its first reduction.
 // U = 1 measured best: with 40 warps resident per SM there is enough memory
 // parallelism, and the smaller CTAs fill the last partial wave better.
+#include <atomic>
+
 #include "wgs_common.cuh"
 
 #ifndef WGS_ROW_WARPS
@@ -148,8 +150,28 @@ __device__ __forceinline__ uint4 add_chunk(const uint4 &a, const uint4 &b) {
     return r;
 }
 
-template <RowOp OP, typename E, int WIDTH, int U, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
+// WGS_ROW_MIN_BLOCKS, when defined: resident CTAs per SM the register
+// allocation must allow (otherwise ptxas chooses)
+#ifdef WGS_ROW_MIN_BLOCKS
+#define WGS_ROW_BOUNDS(T) __launch_bounds__(T, WGS_ROW_MIN_BLOCKS)
+#else
+#define WGS_ROW_BOUNDS(T) __launch_bounds__(T)
+#endif
+
+// Launch shape per op and width.  Most row ops run many short CTAs (the grid
+// capped at WGS_ROW_CTAS_PER_SM per SM, so each SM is refilled as CTAs
+// finish) and prefetch their first iteration's rows before the wait.
+// Norm-gather at width 384 runs one resident wave instead, each CTA
+// prefetching the rows of up to 4 grid-stride iterations: measured on GB300
+// 8.6 -> 8.3 us at [32760,384] -> 34560 rows and 9.1 -> 8.6 us -> 36864
+// rows, while the same shape slowed every other row op by 2-20 %.
+template <RowOp OP, int WIDTH> struct RowLaunch {
+    static constexpr bool kOneWave = OP == RowOp::kNormGather && WIDTH == 384;
+    static constexpr int kPrefetchIters = kOneWave ? 4 : 1;
+};
+
+template <RowOp OP, typename E, int WIDTH, int U, int WARPS, int PF>
+__global__ void WGS_ROW_BOUNDS(WARPS * 32) row_kernel(const RowArgs a) {
 #if !WGS_ROW_EARLY
     pdl_prologue();
 #endif
@@ -175,35 +197,44 @@ __global__ void __launch_bounds__(WARPS * 32) row_kernel(const RowArgs a) {
 
 #if WGS_ROW_EARLY
     // Before waiting for the previous grid, ask L2 for the lines the first
-    // iteration will load.  The rows of direct ops are known; an index-driven
-    // op reads its index first (L2 only) and prefetches the rows it names.
-    // Nothing read here feeds a result: the previous grid may still be
-    // writing these buffers, so the index is read again after the wait and
-    // every row is loaded after it.  Measured on GB300: the C = 384 gather
-    // 9.5 -> 8.1 us, its norm-gather 9.7 -> 8.6 us, every row op 2-10 %.
+    // PF iterations will load.  The rows of direct ops are known; an
+    // index-driven op reads its index first (L2 only) and prefetches the
+    // rows it names.  Nothing read here feeds a result: the previous grid may
+    // still be writing these buffers, so the index is read again after the
+    // wait and every row is loaded after it.  Measured on GB300: the C = 384
+    // gather 9.5 -> 8.1 us, its norm-gather 9.7 -> 8.6 us, every row op 2-10 %.
+    auto prefetch_rows = [&](const int64_t base) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int64_t r = base0 + static_cast<int64_t>(warp * U + u) * RPW + grp;
-        if (r >= a.rows) continue;
-        if constexpr (kByIndex || OP == RowOp::kRevAddLN) {
-            const int64_t s = ld_cg_i32(a.idx + r);
-            if (s >= 0 && s < a.n_src) {
-                const uint16_t *p = kByIndex ? a.in0 : a.in1;
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = base + static_cast<int64_t>(warp * U + u) * RPW + grp;
+            if (r >= a.rows) continue;
+            if constexpr (kByIndex || OP == RowOp::kRevAddLN) {
+                const int64_t s = ld_cg_i32(a.idx + r);
+                if (s >= 0 && s < a.n_src) {
+                    const uint16_t *p = kByIndex ? a.in0 : a.in1;
 #pragma unroll
-                for (int k = 0; k < CPL; ++k) prefetch_l2(p + s * WIDTH + (sub + k * LPR) * 8);
-                if constexpr (OP == RowOp::kAddNormGather)
+                    for (int k = 0; k < CPL; ++k) prefetch_l2(p + s * WIDTH + (sub + k * LPR) * 8);
+                    if constexpr (OP == RowOp::kAddNormGather)
+#pragma unroll
+                        for (int k = 0; k < CPL; ++k)
+                            prefetch_l2(a.in1 + s * WIDTH + (sub + k * LPR) * 8);
+                }
+            }
+            if constexpr (!kByIndex) {
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) prefetch_l2(a.in0 + r * WIDTH + (sub + k * LPR) * 8);
+                if constexpr (OP == RowOp::kAddLN)
 #pragma unroll
                     for (int k = 0; k < CPL; ++k)
-                        prefetch_l2(a.in1 + s * WIDTH + (sub + k * LPR) * 8);
+                        prefetch_l2(a.in1 + r * WIDTH + (sub + k * LPR) * 8);
             }
         }
-        if constexpr (!kByIndex) {
+    };
+    if constexpr (PF == 1) {
+        prefetch_rows(base0);
+    } else {
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) prefetch_l2(a.in0 + r * WIDTH + (sub + k * LPR) * 8);
-            if constexpr (OP == RowOp::kAddLN)
-#pragma unroll
-                for (int k = 0; k < CPL; ++k) prefetch_l2(a.in1 + r * WIDTH + (sub + k * LPR) * 8);
-        }
+        for (int it = 0; it < PF; ++it) prefetch_rows(base0 + it * stride);
     }
     pdl_prologue();
 #endif
@@ -310,9 +341,23 @@ wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     constexpr int U = WGS_ROW_U, WARPS = WGS_ROW_WARPS;
     constexpr int ROWS_CTA = WARPS * (32 / RowTiling<WIDTH>::kLPR) * U;
     const int64_t iters = ceil_div(a.rows, ROWS_CTA);
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
+    using L = RowLaunch<OP, WIDTH>;
+    auto kernel = row_kernel<OP, E, WIDTH, U, WARPS, L::kPrefetchIters>;
+    int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
+    if constexpr (L::kOneWave) {
+        static std::atomic<int> resident[64];  // per device, for this instantiation
+        int per_sm = resident[dev.device].load(std::memory_order_relaxed);
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, WARPS * 32, 0) !=
+                    cudaSuccess ||
+                per_sm < 1)
+                return WGS_ERR_LAUNCH;
+            resident[dev.device].store(per_sm, std::memory_order_relaxed);
+        }
+        cap = static_cast<int64_t>(dev.sm_count) * per_sm;
+    }
     const unsigned grid = static_cast<unsigned>(iters < cap ? iters : cap);
-    return launch(row_kernel<OP, E, WIDTH, U, WARPS>, dim3(grid), dim3(WARPS * 32), 0, stream, a);
+    return launch(kernel, dim3(grid), dim3(WARPS * 32), 0, stream, a);
 }
 
 template <RowOp OP, typename E = Fp16>
