@@ -234,14 +234,8 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
 // every SM fed as CTAs finish, with no index division anywhere.
 constexpr int32_t kRowFormMinVecs = 64;
 
-#ifdef WGS_GELU_ROWS_MIN_CTAS  // optional register cap of the row-block form
-#define WGS_GELU_ROWS_BOUNDS __launch_bounds__(256, WGS_GELU_ROWS_MIN_CTAS)
-#else
-#define WGS_GELU_ROWS_BOUNDS __launch_bounds__(256)
-#endif
-
 template <typename E, int R>
-__global__ void WGS_GELU_ROWS_BOUNDS
+__global__ void __launch_bounds__(256)
 bias_gelu_rows_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
                       int32_t row_vecs, int32_t cv) {
     const int32_t c = static_cast<int32_t>(blockIdx.y) * cv + static_cast<int32_t>(threadIdx.x);
