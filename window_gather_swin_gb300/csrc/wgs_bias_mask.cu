@@ -14,15 +14,13 @@
 //
 // Layout: a logits row is n 16-bit elements = n/8 16-byte chunks.  A CTA of
 // RP x (n/8) threads gives every thread one fixed chunk column and RP rows
-// per pass, U passes in flight.  The grid strides over units, each a
-// contiguous run of rows of one (window, head) tile: a tile's passes are
-// split into the fewest parts of at most WGS_BM_PART_PASSES passes, evened
-// out (n = 144, RP = 7, U = 2: 11 passes in parts of 56, 56 and 32 rows).
+// per pass, U passes in flight.  A CTA takes one unit, a contiguous run of
+// rows of one (window, head) tile: a tile's passes are split into the
+// fewest parts of at most WGS_BM_PART_PASSES passes, evened out (n = 144,
+// RP = 7, U = 2: 11 passes in parts of 56, 56 and 32 rows).
 // A unit's window and head come from two
 // divisions by invariant integers done as multiply-high (Granlund &
 // Montgomery 1994); its window type and column labels are loaded once.
-#include <atomic>
-
 #include "wgs_common.cuh"
 
 #ifndef WGS_BM_EARLY
@@ -97,10 +95,11 @@ __device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t
     return (c_lo != row ? (mask2 & 0xffffu) : 0u) | (c_hi != row ? (mask2 & 0xffff0000u) : 0u);
 }
 
-// The grid strides over units: one (window, head) tile's rows
-// [part * part_rows, (part + 1) * part_rows).  A unit's window type, column
-// labels and base addresses are found once; its rows then stream with plain
-// offsets, U passes of RP rows in flight.
+// A unit is one (window, head) tile's rows [part * part_rows, (part + 1) *
+// part_rows); the launch gives each CTA one (the loop also serves a smaller
+// grid).  A unit's window type, column labels and base addresses are found
+// once; its rows then stream with plain offsets, U passes of RP rows in
+// flight.
 template <typename E, int U>
 __global__ void __launch_bounds__(kMaxChunksPerRow > WGS_BM_THREADS ? kMaxChunksPerRow : WGS_BM_THREADS)
 bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
@@ -219,20 +218,6 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
         constexpr int U = WGS_BM_U;
         const int32_t rp = cpr < WGS_BM_THREADS ? WGS_BM_THREADS / cpr : 1;
         auto kernel = bias_mask_vec<E, U>;
-        // resident CTAs per SM for this CTA size, cached per device as
-        // (threads << 32 | CTAs)
-        static std::atomic<int64_t> resident[64];
-        const int threads = rp * cpr;
-        int64_t cached = resident[dev.device].load(std::memory_order_relaxed);
-        int per_sm = static_cast<int>(cached & 0xffffffff);
-        if ((cached >> 32) != threads || per_sm < 1) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
-                    cudaSuccess ||
-                per_sm < 1)
-                return WGS_ERR_LAUNCH;
-            resident[dev.device].store((static_cast<int64_t>(threads) << 32) | per_sm,
-                                       std::memory_order_relaxed);
-        }
         // the fewest parts of at most WGS_BM_PART_PASSES passes, evened out
         const int32_t passes = static_cast<int32_t>(ceil_div(n, rp * U));
         const int32_t part_passes = static_cast<int32_t>(
@@ -240,8 +225,9 @@ wgs_status launch_bias_mask(const void *scores, const void *bias, const int32_t 
         const int32_t part_rows = part_passes * rp * U;
         const int32_t parts = static_cast<int32_t>(ceil_div(n, part_rows));
         const int64_t units = n_win * heads * parts;
-        const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
-        return launch(kernel, dim3(static_cast<unsigned>(units < cap ? units : cap)),
+        // a CTA per unit: the hardware refills each SM as CTAs finish (one
+        // resident wave striding over units left its last round part-empty)
+        return launch(kernel, dim3(static_cast<unsigned>(units)),
                       dim3(static_cast<unsigned>(rp * cpr)), 0, stream,
                       static_cast<const uint4 *>(scores), static_cast<const uint4 *>(bias),
                       win_type, region, static_cast<uint4 *>(out),
