@@ -556,7 +556,12 @@ def cpu_legs(calls, gpu_outs, want_baseline, want_parity):
     over all usable cores, three repetitions, median) and the parity gate
     (every output element the timed buffers hold against Run 2's outputs)."""
     cores, model = host_cpu()
-    calls = [c for c in calls if c.oracle is not None]
+    keep = [j for j, c in enumerate(calls) if c.oracle is not None]
+    calls = [calls[j] for j in keep]
+    if gpu_outs is not None:
+        gpu_outs = [gpu_outs[j] for j in keep]
+    if not calls:
+        return None, None
     base = parity = None
     last = None
     if want_baseline:

@@ -134,3 +134,18 @@ def test_reference_arm_never_loads_the_cuda_library():
     assert json.loads(lines[-1]) == {"wgs": False}
     ref = json.loads(lines[0])
     assert ref["impl"] == "reference" and ref["cpu_baseline"]["host_cores"] >= 1
+
+
+def test_cpu_legs_skip_calls_without_an_oracle_leg():
+    """A call without an oracle leg (a --only subset can hold one) leaves the
+    others' GPU outputs matched to their own calls."""
+    calls = [c for c in bench.build_calls(gpu=False) if c.workload == "[32760,384]"]
+    assert [c.name for c in calls] == ["ln_fwd", "residual_add_ln_fwd"]
+    _, _, outs = bench.oracle_step(calls, 2, 1.0)
+    gpu = _stitch(outs)
+    extra = bench.Call("no_leg", "x", 0, {}, {}, None, None, 0)
+    base, parity = bench.cpu_legs([calls[0], extra, calls[1]], [gpu[0], None, gpu[1]],
+                                  want_baseline=False, want_parity=True)
+    assert base is None
+    assert parity["pass"], parity.get("failures")
+    assert parity["elements"] == sum(v.size for g in gpu for v in g.values())
