@@ -180,6 +180,34 @@ def test_norm_gather_full_size(stage):
     print("norm_gather", stage.name, st)
 
 
+@pytest.mark.parametrize("width", [192, 384])
+@pytest.mark.parametrize("n_idx", [1, 7, 9, 17, 12163, 40001, 100003])
+def test_norm_gather_ragged_random_maps(width, n_idx):
+    """Random maps with pads and repeated sources at row counts from one row
+    to past what one resident wave covers with its prefetched iterations
+    (norm-gather at width 384 launches one wave of 8-row CTAs and prefetches
+    four grid-stride iterations; 100003 rows take more), in fp16 and bf16."""
+    from parity import LN_TIE_ABS, check_bf16_near
+    n_src = 6000
+    for dt, seed in ((torch.float16, 21), (torch.bfloat16, 22)):
+        src = synth.ln_input(n_src, width, seed=seed + width, dtype=dt)
+        idx = synth.random_index(n_idx, n_src, 0.1, seed=n_idx + seed).numpy()
+        dst = wgs.norm_gather(src.to(DEV), torch.from_numpy(idx).to(DEV), EPS)
+        fmt = "f16" if dt == torch.float16 else "bf16"
+        s_o = src.numpy() if fmt == "f16" else _bits(src)
+        want, bad = oracle.norm_gather(s_o, idx, EPS, fmt=fmt)
+        assert bad == 0
+        src64 = oracle.ln_f64(s_o, EPS, fmt=fmt)
+        want64 = np.where((idx >= 0)[:, None], src64[np.maximum(idx, 0)], 0.0)
+        pad = idx < 0
+        assert not _bits(dst)[pad].any(), "pad rows are not +0"
+        if fmt == "f16":
+            check_ln(np_(dst), want, want64, f"norm_gather {width} x {n_idx}")
+        else:
+            check_bf16_near(_bits(dst), want, want64, f"norm_gather bf16 {width} x {n_idx}",
+                            tie_abs=LN_TIE_ABS)
+
+
 def _iota_rows(n, width):
     rng = np.random.default_rng(n)
     bits = rng.integers(0, 65536, (n, width), dtype=np.uint32).astype(np.uint16)
