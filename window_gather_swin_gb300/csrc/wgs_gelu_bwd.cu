@@ -325,8 +325,8 @@ gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, floa
 // Pass 2: grad_bias[c] = round(sum over slabs of partial[slab][c]).  A CTA
 // takes 32 columns; its 32 slab lanes (one warp each, reading 32
 // consecutive columns of a slab) each sum slabs k, k + 32, ... in order,
-// 16 loads in flight, then the lane sums combine in lane order.  The order
-// is fixed, so the result is deterministic.
+// up to 16 loads in flight at any slab count, then the lane sums combine in
+// lane order.  The order is fixed, so the result is deterministic.
 constexpr int kBiasCols = 32, kBiasLanes = 32, kBiasUnroll = 16;
 
 template <typename E>
@@ -338,16 +338,18 @@ gelu_bwd_bias(const float *partial, void *grad_bias, int32_t width, int32_t slab
     const int32_t c = static_cast<int32_t>(blockIdx.x) * kBiasCols + col;
     float s = 0.f;
     if (c < width) {
-        int32_t q = lane;
-        for (; q + (kBiasUnroll - 1) * kBiasLanes < slabs; q += kBiasUnroll * kBiasLanes) {
+        // up to kBiasUnroll loads in flight, added in slab order
+        for (int32_t q = lane; q < slabs; q += kBiasUnroll * kBiasLanes) {
             float v[kBiasUnroll];
 #pragma unroll
-            for (int u = 0; u < kBiasUnroll; ++u)
-                v[u] = __ldcg(partial + static_cast<int64_t>(q + u * kBiasLanes) * width + c);
+            for (int u = 0; u < kBiasUnroll; ++u) {
+                const int32_t k = q + u * kBiasLanes;
+                v[u] = k < slabs ? __ldcg(partial + static_cast<int64_t>(k) * width + c) : 0.f;
+            }
 #pragma unroll
-            for (int u = 0; u < kBiasUnroll; ++u) s += v[u];
+            for (int u = 0; u < kBiasUnroll; ++u)
+                if (q + u * kBiasLanes < slabs) s += v[u];
         }
-        for (; q < slabs; q += kBiasLanes) s += __ldcg(partial + static_cast<int64_t>(q) * width + c);
     }
     red[lane][col] = s;
     __syncthreads();
