@@ -28,6 +28,13 @@
  *     memory, never synchronises the stream and never touches the default
  *     stream unless the caller passes it (stream 0).
  *   - Work is enqueued on `stream`; the call returns once it is enqueued.
+ *     Kernels are launched with programmatic dependent launch: one may be
+ *     scheduled while the previous kernel on the stream drains, and before
+ *     waiting for it may ask L2 to fetch the lines of its first input rows
+ *     (an index-driven kernel also reads its first index entries, L2 only,
+ *     to steer those fetches).  No value read before the previous kernel
+ *     has completed reaches a result: indices and rows are read again after
+ *     the wait, so the usual stream order holds for every buffer.
  *   - Arguments are checked before anything is launched; a failed check
  *     returns a status and launches nothing.  A launch failure reported by
  *     the runtime returns WGS_ERR_LAUNCH.
