@@ -284,11 +284,11 @@ wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bia
  * owns every allocation and passes its plugins no allocator or workspace,
  * or a hot path that must not call cudaMalloc because that call can
  * synchronise the device.  The partial column sums then live in one array
- * of 1,048,576 floats (4 MiB) built into the library, which every GPU that
+ * of 1,310,720 floats (5 MiB) built into the library, which every GPU that
  * loads the library keeps until the process exits.
  *   Arguments, results and errors as bias_gelu_tanh_bwd, without
  *   `workspace`.  Sizes whose partial sums would not fit (more than
- *   1,048,576 floats: min(512, ceil(rows / 108)) slabs x width, so any row
+ *   1,310,720 floats: min(608, ceil(rows / 108)) slabs x width, so any row
  *   count up to width 2048) return WGS_ERR_TOO_LARGE and launch nothing.
  *   Allocates nothing.  Every call looks up the array's device address in
  *   the calling thread's current context (cudaGetSymbolAddress, a host-side

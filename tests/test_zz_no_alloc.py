@@ -59,13 +59,13 @@ def test_noalloc_backward_matches_the_workspace_entry_point_twice(dtype, rows, w
 
 
 def test_noalloc_backward_larger_then_smaller_shapes_read_no_stale_partials():
-    """The first call fills the whole array (512 slabs x 2048 columns, the
-    largest size it takes); each later call has fewer slabs, a narrower row
-    or the scalar path, and new inputs.  A partial sum left by an earlier
+    """The first call fills as much of the array as any call can (608 slabs
+    x 2048 columns); each later call has fewer slabs, a narrower row or the
+    scalar path, and new inputs.  A partial sum left by an earlier
     call and read again would change grad_bias, so every result must equal
     the workspace entry point's bit for bit."""
     lib = _capi.load()
-    cases = [(torch.float16, 60000, 2048, 50), (torch.float16, 5000, 1024, 51),
+    cases = [(torch.float16, 65664, 2048, 50), (torch.float16, 5000, 1024, 51),
              (torch.float32, 777, 520, 52), (torch.bfloat16, 333, 13, 53)]
     with torch.cuda.device(DEV):
         for dtype, rows, width, seed in cases:
@@ -84,7 +84,7 @@ def test_noalloc_backward_larger_then_smaller_shapes_read_no_stale_partials():
 
 def test_noalloc_backward_refuses_sizes_beyond_its_array():
     lib = _capi.load()
-    rows, width = 100_000, 4096                   # 512 slabs x 4096 columns > 2^20 floats
+    rows, width = 100_000, 4096       # 608 slabs x 4096 columns > the array's 1,310,720 floats
     x = torch.zeros(rows, width, device=DEV)
     b = torch.zeros(width, device=DEV)
     gx = torch.full_like(x, 7.0)
