@@ -792,7 +792,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "storage_dtype": "fp16 rows (LN, gathers, fp16 GELU), fp32 (fp32 GELU)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": step_config(world, args.only, len(calls)),
+        "config": step_config(world, args.only, len(calls), step_bytes=step_bytes, n_sets=n_sets),
         "l2": (f"inputs larger than L2: steps run back to back and one step touches "
                f"{step_bytes * n_sets / 1e6:.0f} MB over {n_sets} buffer set(s) "
                f"(L2 {l2 / 1e6:.0f} MB), so every input is read from HBM; no flush"),
@@ -827,10 +827,15 @@ def run_ours(args, rank, world, local):
         raise SystemExit("parity gate failed: " + "; ".join(parity.get("failures", [])))
 
 
-def step_config(world, only=None, launches=10, rank0_only=False):
-    """The `config` both arms print: the workload and how it is spread."""
+def step_config(world, only=None, launches=10, rank0_only=False, step_bytes=0, n_sets=1):
+    """The `config` both arms print: the workload, how its inputs relate to
+    the GPU's L2 (a property of the workload: both arms state it alike) and
+    how it is spread."""
     cfg = dict(STEP_CONFIG) if not only else {"workload": f"subset: {only}"}
     cfg["launches_per_step"] = launches
+    cfg["l2"] = (f"inputs larger than L2, no flush: steps run back to back and one step touches "
+                 f"{step_bytes / 1e6:.0f} MB over {n_sets} buffer set(s), over 3x a GB300's "
+                 f"L2, so every input is read from HBM")
     cfg["parallelism"] = f"rank 0 of {world}" if rank0_only and world > 1 else f"replicas x{world}"
     return cfg
 
@@ -1039,7 +1044,8 @@ def run_reference(args, rank, world):
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded N(0,1)-family tensors of the stage shapes)",
-        "config": step_config(world, None, len(calls), rank0_only=True),
+        "config": step_config(world, None, len(calls), rank0_only=True,
+                              step_bytes=sum(c.bytes for c in calls)),
         "timing": ("each step runs the oracle on every call of the step (see cpu_baseline.sample); "
                    "time.perf_counter around each call"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
