@@ -1023,9 +1023,9 @@ def run_reference(args, rank, world):
             return
     calls = build_calls(gpu=False)
     cores, model = host_cpu()
-    probe = 1.0 / 256
-    probe_s, _, _ = oracle_step(calls, cores, probe)
-    full_step_s = probe_s / probe
+    # one whole step, untimed, sizes the sample (a small probe would be
+    # dominated by the per-call cost of the thread pool)
+    full_step_s, _, _ = oracle_step(calls, cores, 1.0)
     frac = args.ref_budget_s / (full_step_s * (args.steps + args.warmup))
     frac = max(1.0 / 16384, min(1.0, frac))
     for _ in range(args.warmup):
