@@ -29,6 +29,7 @@
 // format, so results do not depend on the device.  Both passes stream:
 // grad_y and x are read once and grad_x is written once; the partials are a
 // few MB at most.
+#include <atomic>
 #include <type_traits>
 
 #include "wgs_common.cuh"
@@ -49,6 +50,12 @@
 #endif
 #ifndef WGS_BWD_MIN_BLOCKS
 #define WGS_BWD_MIN_BLOCKS 2  // pass-1 CTAs of the largest size kept resident per SM
+#endif
+#ifndef WGS_BWD_ASYNC
+#define WGS_BWD_ASYNC 1  // 16-bit pass 1 stages its next step in shared memory (cp.async)
+#endif
+#ifndef WGS_BWD_ASYNC_STAGES
+#define WGS_BWD_ASYNC_STAGES 2  // ring slots per thread on that path (a power of two)
 #endif
 #ifndef WGS_BWD_MIN_SLAB_ROWS
 // slab count = min(608, ceil(rows / this)): 32760 rows give 304 slabs, which
@@ -282,6 +289,113 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     }
 }
 
+// 16-byte copy global -> shared that bypasses L1 and registers.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Pass 1 for 16-bit data with the next step's chunks staged in shared
+// memory: the same rows, columns, arithmetic and summation order as
+// gelu_bwd_chunks (so the same bits), but each thread copies its own grad_y
+// and x chunks S - 1 steps ahead into its own slots of a ring (cp.async: no
+// registers held), reads them back after cp.async.wait_group, and needs no
+// barrier until the ring is reused for the row-group sums.  With S = 2 (one
+// step ahead, as the register form) the 16-bit kernel no longer spills at
+// its 80-register cap: [32760,1536] 54.1 -> 52.2 us on GB300.  Deeper rings
+// (S = 4: 56.1 us), four rows a step (54.4), one row a step (53.3) and a
+// third CTA per SM at a 56-register cap (59.3) were slower.
+template <typename E, int R, int S>
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
+gelu_bwd_chunks_async(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx,
+                      float *partial, int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb,
+                      int32_t groups, int32_t slabs) {
+    static_assert((S & (S - 1)) == 0, "ring slots must be a power of two");
+    constexpr int kN = 8;
+    extern __shared__ uint4 ring[];  // [S][R][2][blockDim]; then float red[groups][cvb][kN]
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int j = tid % cvb, g = tid / cvb;
+    const int32_t cv = static_cast<int32_t>(blockIdx.y) * cvb + j;
+    const bool active = g < groups && cv < row_chunks;
+    const int64_t r0 = rows * blockIdx.x / slabs, r1 = rows * (blockIdx.x + 1) / slabs;
+    const int64_t first = r0 + g;
+#if WGS_BWD_EARLY
+    if (active) {
+        prefetch_l2(bias + cv);
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (first + q * groups < r1) {
+                prefetch_l2(gy + (first + q * groups) * row_chunks + cv);
+                prefetch_l2(x + (first + q * groups) * row_chunks + cv);
+            }
+    }
+#endif
+    pdl_prologue();
+    float2 acc[kN / 2];
+#pragma unroll
+    for (int e = 0; e < kN / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+    if (active) {
+        const uint4 bv = __ldg(bias + cv);
+        // this thread's rows: first, first + G, ... below r1, R a step
+        const int32_t n_rows = first < r1 ? static_cast<int32_t>((r1 - first + groups - 1) / groups) : 0;
+        const int32_t steps = (n_rows + R - 1) / R;
+        const uint4 *gyp = gy + first * row_chunks + cv;
+        const uint4 *xp = x + first * row_chunks + cv;
+        uint4 *gxp = gx + first * row_chunks + cv;
+        const int64_t rstride = static_cast<int64_t>(groups) * row_chunks;  // chunks between rows
+        auto issue = [&](int32_t st) {
+            const int slot = st & (S - 1);
+#pragma unroll
+            for (int q = 0; q < R; ++q) {
+                const int32_t k = st * R + q;  // the thread's k-th row
+                if (st < steps && k < n_rows) {
+                    cp_async16(&ring[((slot * R + q) * 2 + 0) * nt + tid], gyp + k * rstride);
+                    cp_async16(&ring[((slot * R + q) * 2 + 1) * nt + tid], xp + k * rstride);
+                }
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int st = 0; st < S - 1; ++st) issue(st);
+        for (int32_t st = 0; st < steps; ++st) {
+            issue(st + S - 1);
+            cp_async_wait<S - 1>();  // step st's copies have landed
+            const int slot = st & (S - 1);
+#pragma unroll
+            for (int q = 0; q < R; ++q) {
+                const int32_t k = st * R + q;
+                if (k < n_rows) {
+                    const uint4 gyv = ring[((slot * R + q) * 2 + 0) * nt + tid];
+                    const uint4 xv = ring[((slot * R + q) * 2 + 1) * nt + tid];
+                    st_stream(gxp + k * rstride, grad_chunk<E, true>(gyv, xv, bv, acc));
+                }
+            }
+        }
+        cp_async_wait<0>();
+    }
+    __syncthreads();  // the ring is free: reuse it for the row-group sums
+    float *red = reinterpret_cast<float *>(ring);
+    if (g < groups)
+#pragma unroll
+        for (int e = 0; e < kN; ++e) red[(g * cvb + j) * kN + e] = e & 1 ? acc[e / 2].y : acc[e / 2].x;
+    __syncthreads();
+    if (g == 0 && cv < row_chunks) {
+#pragma unroll
+        for (int e = 0; e < kN; ++e) {
+            float v = red[j * kN + e];
+            for (int q = 1; q < groups; ++q) v += red[(q * cvb + j) * kN + e];
+            partial[static_cast<int64_t>(blockIdx.x) * width + cv * kN + e] = v;
+        }
+    }
+}
+
 // Pass 1, any width / alignment: thread (g, j) owns column blockIdx.y*CVB + j.
 template <typename E>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
@@ -373,7 +487,8 @@ int64_t slabs_for(int64_t rows) {
 
 template <typename E>
 wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx, void *gb,
-                      float *partial, int64_t rows, int32_t width, cudaStream_t stream) {
+                      float *partial, int64_t rows, int32_t width, int device,
+                      cudaStream_t stream) {
     constexpr bool k16 = !std::is_same<E, F32>::value;
     constexpr int kVec = k16 ? 8 : 4;
     const int32_t slabs = static_cast<int32_t>(slabs_for(rows));
@@ -391,7 +506,33 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
     const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(col_blocks));
     const dim3 block(static_cast<unsigned>(cvb * groups));
     wgs_status st;
-    if (chunks) {
+    bool staged = false;
+    if constexpr (k16 && WGS_BWD_ASYNC) {
+        if (chunks) {
+            staged = true;
+            constexpr int R = WGS_BWD_ROWS, S = WGS_BWD_ASYNC_STAGES;
+            auto kernel = gelu_bwd_chunks_async<E, R, S>;
+            const size_t ring = static_cast<size_t>(S) * R * 2 * block.x * sizeof(uint4);
+            const size_t red = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
+            const size_t smem = ring > red ? ring : red;
+            // shared memory above 48 KB needs an opt-in, once per device and size
+            static std::atomic<size_t> opted[64];
+            if (opted[device].load(std::memory_order_relaxed) < smem) {
+                if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem)) != cudaSuccess) {
+                    cudaGetLastError();
+                    return WGS_ERR_LAUNCH;
+                }
+                opted[device].store(smem, std::memory_order_relaxed);
+            }
+            st = launch(kernel, grid, block, smem, stream, static_cast<const uint4 *>(gy),
+                        static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
+                        static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups, slabs);
+        }
+    }
+    if (staged) {
+        // pass 1 is launched
+    } else if (chunks) {
         const size_t smem = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
         st = launch(gelu_bwd_chunks<E, WGS_BWD_ROWS>, grid, block, smem, stream,
                     static_cast<const uint4 *>(gy), static_cast<const uint4 *>(x),
@@ -425,11 +566,14 @@ wgs_status bias_gelu_bwd_checked(const void *grad_y, const void *x, const void *
     if (st != WGS_OK) return st;
     switch (dtype) {
         case WGS_F16:
-            return launch_bwd<Fp16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+            return launch_bwd<Fp16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width,
+                                    dev.device, stream);
         case WGS_BF16:
-            return launch_bwd<Bf16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+            return launch_bwd<Bf16>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width,
+                                    dev.device, stream);
         default:
-            return launch_bwd<F32>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width, stream);
+            return launch_bwd<F32>(grad_y, x, bias, grad_x, grad_bias, partial, rows, width,
+                                   dev.device, stream);
     }
 }
 
