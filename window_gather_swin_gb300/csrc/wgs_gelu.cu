@@ -23,8 +23,10 @@
 //
 // The op streams 2 x rows x width elements through HBM; the vector path
 // moves 16-byte chunks.  Rows of at least 64 chunks run as short CTAs of R
-// rows x one column block, a thread per column chunk; narrower rows run a
-// one-wave grid-stride kernel with U chunks in flight per thread.  Bias
+// rows x one column block, a thread per column chunk (16-bit data: two
+// steps of R rows, the second staged in shared memory while the first
+// computes); narrower rows run a one-wave grid-stride kernel with U chunks
+// in flight per thread.  Bias
 // chunks come through L1 (the whole bias row is at most a few KB).
 #include <atomic>
 #include <type_traits>
@@ -33,6 +35,9 @@
 
 #ifndef WGS_GELU_EARLY
 #define WGS_GELU_EARLY 1  // row-block form: L2 prefetch of the first chunks before the wait
+#endif
+#ifndef WGS_GELU_STAGED_STEPS
+#define WGS_GELU_STAGED_STEPS 2  // 16-bit row-block CTAs of this many steps of R rows, staged (0: off)
 #endif
 #ifndef WGS_GELU_THREADS
 #define WGS_GELU_THREADS 256
@@ -44,7 +49,7 @@
 #define WGS_GELU_U16 2  // chunks per thread per pass for 16-bit data, with prefetch
 #endif
 #ifndef WGS_GELU_R16
-#define WGS_GELU_R16 4  // rows per thread in the row-block form, 16-bit data
+#define WGS_GELU_R16 3  // rows per step in the row-block form, 16-bit data
 #endif
 #ifndef WGS_GELU_R32
 #define WGS_GELU_R32 4  // rows per thread in the row-block form, fp32
@@ -262,6 +267,71 @@ bias_gelu_rows_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
         if (r0 + q < rows) st_stream(y + (r0 + q) * row_vecs + c, gelu_chunk<E>(xv[q], bv));
 }
 
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Row-block form with STEPS steps of R rows per CTA, for 16-bit data: the
+// next step's chunks are copied into shared memory (each thread its own
+// slots, cp.async) while this step computes, so a CTA overlaps its own loads
+// with its arithmetic without holding the next step in registers.  Eight
+// elements a chunk make the arithmetic long; with all of a CTA's rows loaded
+// at once (the plain row-block form, 4 rows) the loads of other CTAs did not
+// cover it.  Measured on GB300 at [32760,1536]: 32.8 -> 30.5 us with 2 steps
+// of 3 rows (4 rows: 30.7; 3 steps: 30.9; 2 rows: 31.4).  fp32, with half
+// the arithmetic per chunk, was slower staged (113.2 -> 113.9-114.5 us).
+template <typename E, int R, int STEPS>
+__global__ void __launch_bounds__(256)
+bias_gelu_rows_staged(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
+                      int32_t row_vecs, int32_t cv) {
+    extern __shared__ uint4 ring[];  // [2][R][blockDim]
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int32_t c = static_cast<int32_t>(blockIdx.y) * cv + tid;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R * STEPS;
+#if WGS_GELU_EARLY
+    if (c < row_vecs) {
+        prefetch_l2(bias + c);
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (r0 + q < rows) prefetch_l2(x + (r0 + q) * row_vecs + c);
+    }
+#endif
+    pdl_prologue();
+    if (c >= row_vecs) return;
+    auto issue = [&](int st) {
+        const int slot = st & 1;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t r = r0 + st * R + q;
+            if (st < STEPS && r < rows) cp_async16(&ring[(slot * R + q) * nt + tid], x + r * row_vecs + c);
+        }
+        cp_async_commit();
+    };
+    const uint4 bv = __ldg(bias + c);
+    issue(0);
+#pragma unroll 1
+    for (int st = 0; st < STEPS; ++st) {
+        issue(st + 1);
+        cp_async_wait<1>();
+        const int slot = st & 1;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t r = r0 + st * R + q;
+            if (r < rows)
+                st_stream(y + r * row_vecs + c, gelu_chunk<E>(ring[(slot * R + q) * nt + tid], bv));
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // Any width, any element alignment: one element per thread per step.
 template <typename E>
 __global__ void __launch_bounds__(256)
@@ -294,6 +364,20 @@ wgs_status launch_gelu(const void *x, const void *bias, void *y, int64_t rows, i
         constexpr bool PF = !std::is_same<E, F32>::value;
         constexpr int R = PF ? WGS_GELU_R16 : WGS_GELU_R32;
         const int32_t row_vecs = static_cast<int32_t>(width / kVec);
+        if constexpr (PF && WGS_GELU_STAGED_STEPS > 0) {
+            constexpr int ST = WGS_GELU_STAGED_STEPS;
+            if (row_vecs >= kRowFormMinVecs &&
+                ceil_div(rows, static_cast<int64_t>(R) * ST) <= INT32_MAX) {
+                const int32_t cv = row_vecs <= 256 ? row_vecs : 256;
+                const dim3 grid(static_cast<unsigned>(ceil_div(rows, static_cast<int64_t>(R) * ST)),
+                                static_cast<unsigned>(ceil_div(row_vecs, cv)));
+                const size_t smem = static_cast<size_t>(2) * R * cv * sizeof(uint4);
+                return launch(bias_gelu_rows_staged<E, R, ST>, grid, dim3(static_cast<unsigned>(cv)),
+                              smem, stream, static_cast<const uint4 *>(x),
+                              static_cast<const uint4 *>(bias), static_cast<uint4 *>(y), rows,
+                              row_vecs, cv);
+            }
+        }
         if (row_vecs >= kRowFormMinVecs && ceil_div(rows, static_cast<int64_t>(R)) <= INT32_MAX) {
             const int32_t cv = row_vecs <= 256 ? row_vecs : 256;
             const dim3 grid(static_cast<unsigned>(ceil_div(rows, static_cast<int64_t>(R))),
