@@ -55,7 +55,7 @@
 #define WGS_BWD_ASYNC 1  // 16-bit pass 1 stages its next step in shared memory (cp.async)
 #endif
 #ifndef WGS_BWD_ASYNC_STAGES
-#define WGS_BWD_ASYNC_STAGES 2  // ring slots per thread on that path (a power of two)
+#define WGS_BWD_ASYNC_STAGES 2  // ring slots per thread on that path
 #endif
 #ifndef WGS_BWD_MIN_SLAB_ROWS
 // slab count = min(608, ceil(rows / this)): 32760 rows give 304 slabs, which
@@ -310,14 +310,14 @@ __device__ __forceinline__ void cp_async_wait() {
 // barrier until the ring is reused for the row-group sums.  With S = 2 (one
 // step ahead, as the register form) the 16-bit kernel no longer spills at
 // its 80-register cap: [32760,1536] 54.1 -> 52.2 us on GB300.  Deeper rings
-// (S = 4: 56.1 us), four rows a step (54.4), one row a step (53.3) and a
-// third CTA per SM at a 56-register cap (59.3) were slower.
+// (S = 3: 54.9 us, S = 4: 56.1), three or four rows a step (53.3, 54.4), one
+// row a step (53.3) and a third CTA per SM at a 56-register cap (59.3) were
+// slower.
 template <typename E, int R, int S>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks_async(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx,
                       float *partial, int64_t rows, int32_t row_chunks, int32_t width, int32_t cvb,
                       int32_t groups, int32_t slabs) {
-    static_assert((S & (S - 1)) == 0, "ring slots must be a power of two");
     constexpr int kN = 8;
     extern __shared__ uint4 ring[];  // [S][R][2][blockDim]; then float red[groups][cvb][kN]
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -351,7 +351,7 @@ gelu_bwd_chunks_async(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 
         uint4 *gxp = gx + first * row_chunks + cv;
         const int64_t rstride = static_cast<int64_t>(groups) * row_chunks;  // chunks between rows
         auto issue = [&](int32_t st) {
-            const int slot = st & (S - 1);
+            const int slot = static_cast<int>(static_cast<uint32_t>(st) % S);
 #pragma unroll
             for (int q = 0; q < R; ++q) {
                 const int32_t k = st * R + q;  // the thread's k-th row
@@ -367,7 +367,7 @@ gelu_bwd_chunks_async(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 
         for (int32_t st = 0; st < steps; ++st) {
             issue(st + S - 1);
             cp_async_wait<S - 1>();  // step st's copies have landed
-            const int slot = st & (S - 1);
+            const int slot = static_cast<int>(static_cast<uint32_t>(st) % S);
 #pragma unroll
             for (int q = 0; q < R; ++q) {
                 const int32_t k = st * R + q;
