@@ -22,6 +22,7 @@
 // U = 1 measured best: with 40 warps resident per SM there is enough memory
 // parallelism, and the smaller CTAs fill the last partial wave better.
 #include <atomic>
+#include <type_traits>
 
 #include "wgs_common.cuh"
 
@@ -165,9 +166,14 @@ __device__ __forceinline__ uint4 add_chunk(const uint4 &a, const uint4 &b) {
 // prefetching the rows of up to 4 grid-stride iterations: measured on GB300
 // 8.6 -> 8.3 us at [32760,384] -> 34560 rows and 9.1 -> 8.6 us -> 36864
 // rows, while the same shape slowed every other row op by 2-20 %.
-template <RowOp OP, int WIDTH> struct RowLaunch {
+// Row groups per warp: one, except bfloat16 norm-gather at width 192, where
+// two measured 16.5 -> 16.1 us at 138240 rows (every other op was 1-7 %
+// slower with two).
+template <RowOp OP, typename E, int WIDTH> struct RowLaunch {
     static constexpr bool kOneWave = OP == RowOp::kNormGather && WIDTH == 384;
     static constexpr int kPrefetchIters = kOneWave ? 4 : 1;
+    static constexpr int kRowGroups =
+        OP == RowOp::kNormGather && WIDTH == 192 && std::is_same<E, Bf16>::value ? 2 : WGS_ROW_U;
 };
 
 template <RowOp OP, typename E, int WIDTH, int U, int WARPS, int PF>
@@ -338,10 +344,10 @@ wgs_status launch_rows(const RowArgs &a, cudaStream_t stream) {
     DeviceInfo dev;
     const wgs_status st = current_device(&dev);
     if (st != WGS_OK) return st;
-    constexpr int U = WGS_ROW_U, WARPS = WGS_ROW_WARPS;
+    using L = RowLaunch<OP, E, WIDTH>;
+    constexpr int U = L::kRowGroups, WARPS = WGS_ROW_WARPS;
     constexpr int ROWS_CTA = WARPS * (32 / RowTiling<WIDTH>::kLPR) * U;
     const int64_t iters = ceil_div(a.rows, ROWS_CTA);
-    using L = RowLaunch<OP, WIDTH>;
     auto kernel = row_kernel<OP, E, WIDTH, U, WARPS, L::kPrefetchIters>;
     int64_t cap = static_cast<int64_t>(dev.sm_count) * WGS_ROW_CTAS_PER_SM;
     if constexpr (L::kOneWave) {
