@@ -91,22 +91,6 @@ __device__ __forceinline__ uint32_t div_by(uint32_t x, FastDiv f) {
     return (__umulhi(x, f.m) + x) >> f.l;
 }
 
-__device__ __forceinline__ void cp_async16_cg(void *smem, const void *gmem) {
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async16_ca(void *smem, const void *gmem) {
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // The mask term of one 32-bit word (two elements): m in each half whose
 // column label differs from the row label, +0 elsewhere.
 __device__ __forceinline__ uint32_t mask_word(int32_t row, int32_t c_lo, int32_t c_hi,
@@ -176,7 +160,7 @@ bias_mask_vec(const uint4 *scores, const uint4 *bias, const int32_t *win_type,
             for (int u = 0; u < U; ++u) {
                 const int32_t ii = i0 + pass * rp * U + u * rp;
                 if (pass < npass && ii < i1) {
-                    cp_async16_cg(&ring[((slot * U + u) * 2 + 0) * nt + tid], sp + static_cast<int64_t>(ii) * cpr);
+                    cp_async16(&ring[((slot * U + u) * 2 + 0) * nt + tid], sp + static_cast<int64_t>(ii) * cpr);
                     if (ok) cp_async16_ca(&ring[((slot * U + u) * 2 + 1) * nt + tid], bp + static_cast<int64_t>(ii) * cpr);
                 }
             }

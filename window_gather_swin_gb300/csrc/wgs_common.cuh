@@ -102,6 +102,28 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 // load of the same address.
 __device__ __forceinline__ int32_t ld_cg_i32(const int32_t *p) { return __ldcg(p); }
 
+// 16-byte asynchronous copy global -> shared (cp.async; the executing
+// thread reads the slot after cp_async_wait).  cg: cached in L2 only; ca:
+// also in L1, for data other CTAs of the SM reread.  Both addresses must be
+// 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async16_ca(void *smem, const void *gmem) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+// Close the group of copies issued since the last commit.
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 16-byte global load that skips L1 (each byte is read exactly once).
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return __ldcg(reinterpret_cast<const uint4 *>(p));

@@ -207,28 +207,28 @@ bias_gelu_vec_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t n_vec,
             col0 += per_iter;
             if (col0 >= row_vecs) col0 -= row_vecs;
         }
-        return;
-    }
-    for (; i0 < n_vec; i0 += stride) {
-        uint4 xv[U], bv[U];
-        int32_t col = col0;
+    } else {
+        for (; i0 < n_vec; i0 += stride) {
+            uint4 xv[U], bv[U];
+            int32_t col = col0;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
-            if (i < n_vec) {
-                xv[u] = ld_stream(x + i);
-                bv[u] = __ldg(bias + col);
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
+                if (i < n_vec) {
+                    xv[u] = ld_stream(x + i);
+                    bv[u] = __ldg(bias + col);
+                }
+                col += in_tile;
+                if (col >= row_vecs) col -= row_vecs;
             }
-            col += in_tile;
-            if (col >= row_vecs) col -= row_vecs;
-        }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
-            if (i < n_vec) st_stream(y + i, gelu_chunk<E>(xv[u], bv[u]));
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + static_cast<int64_t>(u) * THREADS;
+                if (i < n_vec) st_stream(y + i, gelu_chunk<E>(xv[u], bv[u]));
+            }
+            col0 += per_iter;
+            if (col0 >= row_vecs) col0 -= row_vecs;
         }
-        col0 += per_iter;
-        if (col0 >= row_vecs) col0 -= row_vecs;
     }
 }
 
@@ -265,18 +265,6 @@ bias_gelu_rows_kernel(const uint4 *x, const uint4 *bias, uint4 *y, int64_t rows,
 #pragma unroll
     for (int q = 0; q < R; ++q)
         if (r0 + q < rows) st_stream(y + (r0 + q) * row_vecs + c, gelu_chunk<E>(xv[q], bv));
-}
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Row-block form with STEPS steps of R rows per CTA, for 16-bit data: the

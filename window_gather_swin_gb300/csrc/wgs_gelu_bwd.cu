@@ -289,19 +289,6 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
     }
 }
 
-// 16-byte copy global -> shared that bypasses L1 and registers.
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Pass 1 for 16-bit data with the next step's chunks staged in shared
 // memory: the same rows, columns, arithmetic and summation order as
 // gelu_bwd_chunks (so the same bits), but each thread copies its own grad_y
