@@ -502,9 +502,11 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
             const size_t ring = static_cast<size_t>(S) * R * 2 * block.x * sizeof(uint4);
             const size_t red = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
             const size_t smem = ring > red ? ring : red;
-            // shared memory above 48 KB needs an opt-in, once per device and size
+            // shared memory above 48 KB needs an opt-in, once per device and
+            // size (two slots of two rows at 384 threads need exactly 48 KB,
+            // so the shipped configuration never asks)
             static std::atomic<size_t> opted[64];
-            if (opted[device].load(std::memory_order_relaxed) < smem) {
+            if (smem > 48 * 1024 && opted[device].load(std::memory_order_relaxed) < smem) {
                 if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem)) != cudaSuccess) {
                     cudaGetLastError();
