@@ -288,7 +288,7 @@ wgs_status bias_gelu_tanh_bwd(const void *grad_y, const void *x, const void *bia
  * loads the library keeps until the process exits.
  *   Arguments, results and errors as bias_gelu_tanh_bwd, without
  *   `workspace`.  Sizes whose partial sums would not fit (more than
- *   1,310,720 floats: min(608, ceil(rows / 108)) slabs x width, so any row
+ *   1,310,720 floats: min(608, ceil(rows / 216)) slabs x width, so any row
  *   count up to width 2048) return WGS_ERR_TOO_LARGE and launch nothing.
  *   Allocates nothing.  Every call looks up the array's device address in
  *   the calling thread's current context (cudaGetSymbolAddress, a host-side

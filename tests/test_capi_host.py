@@ -252,8 +252,9 @@ def test_block_boundary_argument_errors(lib):
 def test_gelu_backward_argument_errors(lib):
     f = lib.bias_gelu_tanh_bwd
     need = lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 768)
-    assert need == 10 * 768 * 4                      # 1000 rows -> ceil(1000 / 108) = 10 slabs
-    assert lib.wgs_bias_gelu_bwd_workspace_bytes(131040, 768) == 608 * 768 * 4   # the slab cap
+    assert need == 5 * 768 * 4                       # 1000 rows -> ceil(1000 / 216) = 5 slabs
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(131040, 768) == 607 * 768 * 4   # ceil(131040 / 216)
+    assert lib.wgs_bias_gelu_bwd_workspace_bytes(200000, 768) == 608 * 768 * 4   # the slab cap
     assert lib.wgs_bias_gelu_bwd_workspace_bytes(0, 768) == 768 * 4   # one slab: grad_bias = 0
     assert lib.wgs_bias_gelu_bwd_workspace_bytes(1000, 0) == 0
     W = 0x50000000

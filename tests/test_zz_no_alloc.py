@@ -65,7 +65,7 @@ def test_noalloc_backward_larger_then_smaller_shapes_read_no_stale_partials():
     call and read again would change grad_bias, so every result must equal
     the workspace entry point's bit for bit."""
     lib = _capi.load()
-    cases = [(torch.float16, 65664, 2048, 50), (torch.float16, 5000, 1024, 51),
+    cases = [(torch.float16, 131328, 2048, 50), (torch.float16, 5000, 1024, 51),
              (torch.float32, 777, 520, 52), (torch.bfloat16, 333, 13, 53)]
     with torch.cuda.device(DEV):
         for dtype, rows, width, seed in cases:
@@ -84,7 +84,7 @@ def test_noalloc_backward_larger_then_smaller_shapes_read_no_stale_partials():
 
 def test_noalloc_backward_refuses_sizes_beyond_its_array():
     lib = _capi.load()
-    rows, width = 100_000, 4096       # 608 slabs x 4096 columns > the array's 1,310,720 floats
+    rows, width = 100_000, 4096       # 463 slabs x 4096 columns > the array's 1,310,720 floats
     x = torch.zeros(rows, width, device=DEV)
     b = torch.zeros(width, device=DEV)
     gx = torch.full_like(x, 7.0)

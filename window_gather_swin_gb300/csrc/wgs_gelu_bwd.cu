@@ -44,12 +44,12 @@
 #define WGS_BWD_GROUPS 4  // most row groups per CTA
 #endif
 #ifndef WGS_BWD_TARGET_THREADS
-// pass-1 threads to aim for when choosing row groups: two 384-thread CTAs on
+// pass-1 threads to aim for when choosing row groups: one 768-thread CTA on
 // each of 152 SMs, all that stay resident at the 80-register cap
 #define WGS_BWD_TARGET_THREADS 116736
 #endif
 #ifndef WGS_BWD_MIN_BLOCKS
-#define WGS_BWD_MIN_BLOCKS 2  // pass-1 CTAs of the largest size kept resident per SM
+#define WGS_BWD_MIN_BLOCKS 1  // pass-1 CTAs of the largest size kept resident per SM
 #endif
 #ifndef WGS_BWD_ASYNC
 #define WGS_BWD_ASYNC 1  // 16-bit pass 1 stages its next step in shared memory (cp.async)
@@ -58,9 +58,9 @@
 #define WGS_BWD_ASYNC_STAGES 2  // ring slots per thread on that path
 #endif
 #ifndef WGS_BWD_MIN_SLAB_ROWS
-// slab count = min(608, ceil(rows / this)): 32760 rows give 304 slabs, which
-// with two row groups fill the resident CTA slots exactly
-#define WGS_BWD_MIN_SLAB_ROWS 108
+// slab count = min(608, ceil(rows / this)): 32760 rows give 152 slabs, which
+// with four row groups fill the resident thread slots exactly
+#define WGS_BWD_MIN_SLAB_ROWS 216
 #endif
 
 namespace wgs {
@@ -78,10 +78,10 @@ constexpr int64_t kMinRowsPerSlab = WGS_BWD_MIN_SLAB_ROWS;
 // slot in one wave (fp32 [131040,768]: 186.9 -> 181.7 us against 512 slabs).
 constexpr int64_t kMaxSlabs = 608;
 constexpr int kMaxChunksPerBlock = 256;  // column chunks per CTA
-// Pass 1 runs at most 384 threads per CTA and keeps two such CTAs per SM
-// resident (at most 85 registers a thread), so the usual grids fit in one
-// wave.
-constexpr int kMaxThreads = 384;
+// Pass 1 runs at most 768 threads per CTA and keeps one such CTA per SM
+// resident (at most 85 registers a thread; the kernels use 78-80, so four
+// 192-thread CTAs fit as well), so the usual grids fit in one wave.
+constexpr int kMaxThreads = 768;
 constexpr int kMinBlocks = WGS_BWD_MIN_BLOCKS;
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -299,7 +299,11 @@ gelu_bwd_chunks(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx, f
 // its 80-register cap: [32760,1536] 54.1 -> 52.2 us on GB300.  Deeper rings
 // (S = 3: 54.9 us, S = 4: 56.1), three or four rows a step (53.3, 54.4), one
 // row a step (53.3) and a third CTA per SM at a 56-register cap (59.3) were
-// slower.
+// slower.  One 768-thread CTA per SM (four row groups over 152 slabs of 216
+// rows) beat two 384-thread CTAs (two groups, 304 slabs of 108 rows): 51.1
+// against 51.5 us, with half as many partial sums for pass 2; five groups at
+// a 64-register cap (960 threads) took 51.9 us (one row a step) or 54.4 (two
+// rows a step, spilling).
 template <typename E, int R, int S>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gelu_bwd_chunks_async(const uint4 *gy, const uint4 *x, const uint4 *bias, uint4 *gx,
@@ -431,12 +435,24 @@ gelu_bwd_scalar(const void *gyp, const void *xp, const void *bp, void *gxp, floa
 // consecutive columns of a slab) each sum slabs k, k + 32, ... in order,
 // up to 16 loads in flight at any slab count, then the lane sums combine in
 // lane order.  The order is fixed, so the result is deterministic.
+//
+// Unlike the other kernels, it lets the next grid launch before its own
+// wait.  That is safe: the next grid's griddepcontrol.wait still waits for
+// this grid to complete, and this grid reads nothing before its own wait.
+// Pass 2 is short and starts only as pass 1 ends, so releasing the next
+// grid after the wait left that grid's launch and first-row prefetches
+// outside any overlap: [32760,1536] 52.2 -> 51.5 us, [131040,768] 182.6 ->
+// 181.7 us.  (Every kernel of the library signalling first measured the
+// same elsewhere.)
 constexpr int kBiasCols = 32, kBiasLanes = 32, kBiasUnroll = 16;
 
 template <typename E>
 __global__ void __launch_bounds__(kBiasCols * kBiasLanes)
 gelu_bwd_bias(const float *partial, void *grad_bias, int32_t width, int32_t slabs) {
-    pdl_prologue();
+#if WGS_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
     __shared__ float red[kBiasLanes][kBiasCols];
     const int col = threadIdx.x % kBiasCols, lane = threadIdx.x / kBiasCols;
     const int32_t c = static_cast<int32_t>(blockIdx.x) * kBiasCols + col;
@@ -503,8 +519,7 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
             const size_t red = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
             const size_t smem = ring > red ? ring : red;
             // shared memory above 48 KB needs an opt-in, once per device and
-            // size (two slots of two rows at 384 threads need exactly 48 KB,
-            // so the shipped configuration never asks)
+            // size (two slots of two rows at 768 threads take 96 KB)
             static std::atomic<size_t> opted[64];
             if (smem > 48 * 1024 && opted[device].load(std::memory_order_relaxed) < smem) {
                 if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
