@@ -793,6 +793,10 @@ def test_identical_results_when_captured_in_a_cuda_graph():
     sc, bb = synth.attention_logits(m.numel() // 144, 2, 144, 1, seed=4)
     sc, bb = sc.to(dev), bb.to(dev)
     reg = wgs.build_shift_regions(st.grid, synth.WINDOW, synth.SHIFT, st.padded).to(dev)
+    hx, hb = synth.gelu_input(300, 1536, torch.float16, seed=12)
+    hg, _ = synth.gelu_input(300, 1536, torch.float16, seed=13)
+    hx, hb, hg = hx.to(dev), hb.to(dev), hg.to(dev)
+    fg = torch.randn(x.shape, generator=torch.Generator().manual_seed(14)).to(dev)
 
     def run(outs):
         wgs.residual_add_ln_fwd(a, b, EPS, residual_out=outs["r"], out=outs["y"])
@@ -804,6 +808,8 @@ def test_identical_results_when_captured_in_a_cuda_graph():
         wgs.window_reverse_add_ln_fwd(a, outs["w"], inv, EPS, residual_out=outs["r3"],
                                       out=outs["y3"])
         wgs.window_bias_mask_add(sc, bb, None, reg, out=outs["s"])
+        wgs.bias_gelu_tanh_bwd(hg, hx, hb, grad_x=outs["hx"], grad_bias=outs["hb"])
+        wgs.bias_gelu_tanh_bwd(fg, x, bias, grad_x=outs["fx"], grad_bias=outs["fb"])
 
     def fresh():
         return {"r2": torch.empty_like(a), "g2": torch.empty(m.numel(), 192, dtype=torch.float16,
@@ -812,7 +818,9 @@ def test_identical_results_when_captured_in_a_cuda_graph():
                 "r": torch.empty_like(a), "y": torch.empty_like(a),
                 "g": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
                 "w": torch.empty(m.numel(), 192, dtype=torch.float16, device=dev),
-                "l": torch.empty_like(xl), "z": torch.empty_like(x), "s": torch.empty_like(sc)}
+                "l": torch.empty_like(xl), "z": torch.empty_like(x), "s": torch.empty_like(sc),
+                "hx": torch.empty_like(hx), "hb": torch.empty_like(hb),
+                "fx": torch.empty_like(x), "fb": torch.empty_like(bias)}
 
     eager = fresh()
     run(eager)
@@ -829,6 +837,47 @@ def test_identical_results_when_captured_in_a_cuda_graph():
     torch.cuda.synchronize(dev)
     for k in eager:
         assert torch.equal(eager[k].view(torch.uint8), graphed[k].view(torch.uint8)), k
+
+
+def test_backward_whose_first_call_is_captured_in_a_graph():
+    """In a fresh process the backward's first call may come inside a
+    stream capture, where its 16-bit pass 1 first raises its shared-memory
+    limit: the replayed graph must give the eager call's bits."""
+    import os
+    import subprocess
+    import sys
+    import textwrap
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = textwrap.dedent("""
+        import sys
+        import torch
+        sys.path.insert(0, sys.argv[1])
+        import window_gather_swin_gb300 as wgs
+        from window_gather_swin_gb300 import _capi, synth
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        x, b = synth.gelu_input(4000, 1536, torch.float16, seed=21)
+        gy, _ = synth.gelu_input(4000, 1536, torch.float16, seed=22)
+        x, b, gy = x.to(dev), b.to(dev), gy.to(dev)
+        gx, gb = torch.full_like(x, float("nan")), torch.full_like(b, float("nan"))
+        need = int(_capi.load().wgs_bias_gelu_bwd_workspace_bytes(4000, 1536))
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            wgs.bias_gelu_tanh_bwd(gy, x, b, grad_x=gx, grad_bias=gb, workspace=ws)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ex, eb = wgs.bias_gelu_tanh_bwd(gy, x, b)
+        torch.cuda.synchronize(dev)
+        assert torch.equal(gx.view(torch.uint8), ex.view(torch.uint8)), "grad_x"
+        assert torch.equal(gb.view(torch.uint8), eb.view(torch.uint8)), "grad_bias"
+        print("captured first call ok")
+    """)
+    r = subprocess.run([sys.executable, "-c", code, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "captured first call ok" in r.stdout, r.stdout + r.stderr
 
 
 # ------------------------------------------------------------ bias-mask ----
