@@ -509,6 +509,38 @@ def test_runs_on_the_callers_stream():
     assert torch.equal(y.view(torch.int16), want.view(torch.int16))
 
 
+def test_backward_outputs_feed_the_next_launches_directly():
+    """The backward's pass 2 lets the next grid launch before it waits, and
+    the library's kernels launch early behind each other: a chain of
+    launches that consume grad_x and grad_bias as soon as they are written,
+    with no synchronisation in between, must give the bits of the same chain
+    run one call at a time."""
+    dev = torch.device(DEV)
+    x, b = synth.gelu_input(32760, 1536, torch.float16, seed=31)
+    gy, _ = synth.gelu_input(32760, 1536, torch.float16, seed=32)
+    x, b, gy = x.to(dev), b.to(dev), gy.to(dev)
+
+    def chain(sync):
+        out = []
+        bb = b
+        for _ in range(3):
+            gx, gb = wgs.bias_gelu_tanh_bwd(gy, x, bb)  # pass 1 writes gx, pass 2 gb
+            if sync:
+                torch.cuda.synchronize(dev)
+            y = wgs.bias_gelu_tanh(gx, gb)              # reads both right away
+            if sync:
+                torch.cuda.synchronize(dev)
+            out += [gx, gb, y]
+            bb = gb                                      # the next backward's bias
+        return out
+
+    want = chain(True)
+    got = chain(False)
+    torch.cuda.synchronize(dev)
+    for k, (w, v) in enumerate(zip(want, got)):
+        assert torch.equal(w.view(torch.int16), v.view(torch.int16)), k
+
+
 def test_concurrent_streams_and_host_threads_give_the_sequential_bits():
     """Different entry points running at once on four streams, launched from
     four host threads, each repeated: every output equals its sequential
