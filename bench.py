@@ -806,6 +806,8 @@ def run_ours(args, rank, world, local):
         "kernels_next": kernels_next,
         "gelu_rows_sweep": sweep,
         "roofline": roofline,
+        "gpu": {"name": torch.cuda.get_device_name(dev), "sms": props.multi_processor_count,
+                "l2_bytes": l2, "cc": f"{props.major}.{props.minor}"},
         "clocks": clocks,
         "gpu_launches": K * len(calls),
         "e2e": e2e,
