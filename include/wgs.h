@@ -51,7 +51,12 @@
  *     needs from the runtime (SM count, resident CTAs per SM), and so does
  *     window_bias_mask_add's first call with a new n; make those calls
  *     outside stream capture.  Other calls, captured or not, make no such
- *     query.  Both depend on the device only, not on its context.
+ *     query.  Both depend on the device only, not on its context.  The
+ *     16-bit GELU backward also raises its first pass's shared-memory limit,
+ *     which belongs to the context: the first call on a device does it, and
+ *     in a later context (after cudaDeviceReset, say) the first launch there
+ *     is rejected by the runtime, the limit raised and the launch retried;
+ *     make that call outside stream capture too.
  */
 #ifndef WGS_H
 #define WGS_H

@@ -14,7 +14,9 @@
  *   - bias_gelu_tanh_bwd_noalloc gives the same bits as bias_gelu_tanh_bwd
  *     with a caller workspace;
  *   - an index outside [-1, n_src) makes wgs_check_error report
- *     WGS_ERR_INDEX, and the next check reports WGS_OK.
+ *     WGS_ERR_INDEX, and the next check reports WGS_OK;
+ *   - after cudaDeviceReset the fp16 backward (with and without a
+ *     workspace) gives the bits it gave before the reset.
  * Prints "device ok" and exits 0, or names the first failed check and
  * exits 1 (2 when no usable device is present).
  */
@@ -45,6 +47,47 @@ static int fails = 0;
     } while (0)
 
 enum { W = 192 };
+
+/* The fp16 backward at [rows, width] through both entry points, on buffers
+ * and a stream made here and released before returning.  Returns 0, or 1
+ * when a CUDA call failed. */
+static int bwd16(int64_t rows, int32_t width, const uint16_t *gy, const uint16_t *x,
+                 const uint16_t *b, uint16_t *gx_ws, uint16_t *gb_ws, uint16_t *gx_na,
+                 uint16_t *gb_na, wgs_status *st_ws, wgs_status *st_na) {
+    const size_t n = (size_t)(rows * width) * 2, nb = (size_t)width * 2;
+    const size_t ws = wgs_bias_gelu_bwd_workspace_bytes(rows, width);
+    cudaStream_t s;
+    void *d_gy, *d_x, *d_b, *d_gx, *d_gb, *d_ws;
+    CUDA(cudaStreamCreate(&s));
+    CUDA(cudaMalloc(&d_gy, n));
+    CUDA(cudaMalloc(&d_x, n));
+    CUDA(cudaMalloc(&d_b, nb));
+    CUDA(cudaMalloc(&d_gx, n));
+    CUDA(cudaMalloc(&d_gb, nb));
+    CUDA(cudaMalloc(&d_ws, ws));
+    CUDA(cudaMemcpy(d_gy, gy, n, cudaMemcpyHostToDevice));
+    CUDA(cudaMemcpy(d_x, x, n, cudaMemcpyHostToDevice));
+    CUDA(cudaMemcpy(d_b, b, nb, cudaMemcpyHostToDevice));
+    *st_ws = bias_gelu_tanh_bwd(d_gy, d_x, d_b, d_gx, d_gb, d_ws, ws, rows, width, WGS_F16, s);
+    CUDA(cudaStreamSynchronize(s));
+    CUDA(cudaMemcpy(gx_ws, d_gx, n, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(gb_ws, d_gb, nb, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemset(d_gx, 0xFF, n));
+    CUDA(cudaMemset(d_gb, 0xFF, nb));
+    *st_na = bias_gelu_tanh_bwd_noalloc(d_gy, d_x, d_b, d_gx, d_gb, rows, width, WGS_F16, s);
+    CUDA(cudaStreamSynchronize(s));
+    CUDA(cudaMemcpy(gx_na, d_gx, n, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(gb_na, d_gb, nb, cudaMemcpyDeviceToHost));
+    cudaFree(d_gy); cudaFree(d_x); cudaFree(d_b); cudaFree(d_gx); cudaFree(d_gb); cudaFree(d_ws);
+    cudaStreamDestroy(s);
+    return 0;
+}
+
+/* A binary16 value in [2^-4, 4) with a random sign and significand. */
+static uint16_t rand_half(void) {
+    const unsigned sign = (unsigned)(rand() & 1), ex = 11u + (unsigned)(rand() % 6);
+    return (uint16_t)((sign << 15) | (ex << 10) | (unsigned)(rand() & 0x3FF));
+}
 
 int main(void) {
     int count = 0;
@@ -171,6 +214,45 @@ int main(void) {
     cudaStreamDestroy(s);
     free(idx); free(src); free(dst); free(x); free(y); free(bx); free(bg); free(bb);
     free(o1); free(o2);
+
+    /* ---- the same results in a new context after a device reset: the fp16
+     * backward at [4000, 1536] runs 768-thread CTAs whose shared-memory limit
+     * is raised per context, and the no-alloc form looks its array up in
+     * the current context ---- */
+    {
+        const int64_t hr = 4000;
+        const int32_t hw = 1536;
+        const size_t hn = (size_t)(hr * hw);
+        uint16_t *h_gy = (uint16_t *)malloc(hn * 2), *h_x = (uint16_t *)malloc(hn * 2);
+        uint16_t h_b[1536];
+        uint16_t *r[4], *rb[4];
+        wgs_status sw[2], sn[2];
+        if (!h_gy || !h_x) return 1;
+        for (size_t i = 0; i < hn; ++i) {
+            h_gy[i] = rand_half();
+            h_x[i] = rand_half();
+        }
+        for (int i = 0; i < hw; ++i) h_b[i] = rand_half();
+        for (int k = 0; k < 4; ++k) {
+            r[k] = (uint16_t *)malloc(hn * 2);
+            rb[k] = (uint16_t *)malloc((size_t)hw * 2);
+            if (!r[k] || !rb[k]) return 1;
+        }
+        if (bwd16(hr, hw, h_gy, h_x, h_b, r[0], rb[0], r[1], rb[1], &sw[0], &sn[0])) return 1;
+        CUDA(cudaDeviceReset());
+        if (bwd16(hr, hw, h_gy, h_x, h_b, r[2], rb[2], r[3], rb[3], &sw[1], &sn[1])) return 1;
+        CHECK(sw[0] == WGS_OK && sn[0] == WGS_OK && sw[1] == WGS_OK && sn[1] == WGS_OK);
+        for (int k = 1; k < 4; ++k) {
+            CHECK(memcmp(r[0], r[k], hn * 2) == 0);
+            CHECK(memcmp(rb[0], rb[k], (size_t)hw * 2) == 0);
+        }
+        for (int k = 0; k < 4; ++k) {
+            free(r[k]);
+            free(rb[k]);
+        }
+        free(h_gy);
+        free(h_x);
+    }
     if (fails) return 1;
     printf("device ok\n");
     return 0;

@@ -518,20 +518,33 @@ wgs_status launch_bwd(const void *gy, const void *x, const void *bias, void *gx,
             const size_t ring = static_cast<size_t>(S) * R * 2 * block.x * sizeof(uint4);
             const size_t red = static_cast<size_t>(groups) * cvb * kVec * sizeof(float);
             const size_t smem = ring > red ? ring : red;
-            // shared memory above 48 KB needs an opt-in, once per device and
-            // size (two slots of two rows at 768 threads take 96 KB)
+            // Shared memory above 48 KB needs an opt-in (two slots of two
+            // rows at 768 threads take 96 KB).  The opt-in belongs to the
+            // context the kernel is loaded in, so the per-device record only
+            // saves the call: a launch the runtime rejects for want of it (in
+            // a new context on the device, e.g. after a reset) raises the
+            // limit there and is retried once.
             static std::atomic<size_t> opted[64];
-            if (smem > 48 * 1024 && opted[device].load(std::memory_order_relaxed) < smem) {
+            auto opt_in = [&]() {
                 if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem)) != cudaSuccess) {
                     cudaGetLastError();
-                    return WGS_ERR_LAUNCH;
+                    return false;
                 }
                 opted[device].store(smem, std::memory_order_relaxed);
-            }
-            st = launch(kernel, grid, block, smem, stream, static_cast<const uint4 *>(gy),
-                        static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
-                        static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups, slabs);
+                return true;
+            };
+            const bool big = smem > 48 * 1024;
+            if (big && opted[device].load(std::memory_order_relaxed) < smem && !opt_in())
+                return WGS_ERR_LAUNCH;
+            auto go = [&]() {
+                return launch(kernel, grid, block, smem, stream, static_cast<const uint4 *>(gy),
+                              static_cast<const uint4 *>(x), static_cast<const uint4 *>(bias),
+                              static_cast<uint4 *>(gx), partial, rows, units, width, cvb, groups,
+                              slabs);
+            };
+            st = go();
+            if (st == WGS_ERR_LAUNCH && big && opt_in()) st = go();
         }
     }
     if (staged) {
