@@ -48,10 +48,9 @@
  *     bias_gelu_tanh_bwd_noalloc).  Kernels name the error words
  *     directly, so no device address is kept between calls.
  *   - The first call of an entry point on a device (per dtype) caches what it
- *     needs from the runtime (SM count, resident CTAs per SM), and so does
- *     window_bias_mask_add's first call with a new n; make those calls
- *     outside stream capture.  Other calls, captured or not, make no such
- *     query.  Both depend on the device only, not on its context.  The
+ *     needs from the runtime (SM count, resident CTAs per SM); make those
+ *     calls outside stream capture.  Other calls, captured or not, make no
+ *     such query.  Both depend on the device only, not on its context.  The
  *     16-bit GELU backward also raises its first pass's shared-memory limit,
  *     which belongs to the context: the first call on a device does it, and
  *     in a later context (after cudaDeviceReset, say) the first launch there
